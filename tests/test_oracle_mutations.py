@@ -1,0 +1,108 @@
+"""Planted mistakes: each test hands a pin a deliberately broken copy of an oracle
+function (on the CPU, in the oracle only) and checks that the pin rejects it.
+This shows the pins would catch a dropped term, a wrong sign, rounding rule,
+index or operand order in the oracle itself."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import csa2, formats as F
+from tests import oracle_pins as P
+
+
+def _fails(check, *args):
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        check(*args)
+
+
+def test_e2m1_ties_away_from_zero_is_caught():
+    def bad(v):
+        v = np.asarray(v, np.float64)
+        a = np.abs(v)
+        d = np.abs(a[..., None] - F.E2M1_MAGNITUDES)
+        code = (d.shape[-1] - 1 - np.argmin(d[..., ::-1], axis=-1)).astype(np.uint8)  # ties upward
+        return code | (np.signbit(v).astype(np.uint8) << 3)
+    _fails(P.check_e2m1_encode, bad)
+
+
+def test_e2m1_dropped_sign_is_caught():
+    _fails(P.check_e2m1_encode, lambda v: F.e2m1_encode(np.abs(np.asarray(v))))
+
+
+def test_e4m3_without_saturation_is_caught():
+    def bad(v):
+        v = np.asarray(v, np.float64)
+        out = F.e4m3_encode(np.minimum(v, 448.0))
+        return np.where(v > 448, np.uint8(0x7F), out)
+    _fails(P.check_e4m3_encode, bad)
+
+
+def test_scale_amax_over_4_is_caught():
+    orig = F.e4m3_encode
+
+    def bad_quant(x):
+        x = np.asarray(x, np.float32)
+        return csa2.quantize_main(x * np.float32(1.5))
+    _fails(P.check_quantize_main_brute, bad_quant)
+    assert F.e4m3_encode is orig
+
+
+def test_indexer_exponent_off_by_one_is_caught(monkeypatch):
+    real = csa2.indexer_shared_exponent
+    monkeypatch.setattr(csa2, "indexer_shared_exponent", lambda a: np.clip(real(a) + 1, -127, 127))
+    _fails(P.check_quantize_indexer, csa2.quantize_indexer, csa2.dequantize_indexer)
+
+
+def test_swapped_nibbles_are_caught():
+    bad = lambda c: (np.asarray(c)[..., 1::2] | (np.asarray(c)[..., 0::2] << 4)).astype(np.uint8)  # noqa: E731
+    _fails(P.check_pack, bad, csa2.unpack_nibbles)
+
+
+def test_merge_with_one_rounding_is_caught():
+    def fused(x0, x1, w0, w1):
+        return (np.asarray(x0, np.float64) * w0 + np.asarray(x1, np.float64) * w1).astype(np.float32)
+    _fails(P.check_merge, fused)
+
+
+def test_merge_with_swapped_weights_is_caught():
+    _fails(P.check_merge, lambda x0, x1, w0, w1: csa2.merge_ratio2(x0, x1, w1, w0))
+
+
+def test_scores_without_relu_or_with_a_dropped_head_are_caught():
+    _fails(P.check_scores, lambda q, w, k: (k @ np.asarray(q).T) @ w)
+    _fails(P.check_scores, lambda q, w, k: np.maximum(k @ np.asarray(q)[:3].T, 0) @ np.asarray(w)[:3])
+
+
+def test_topk_wrong_tie_rule_or_order_is_caught():
+    def ties_high(s, k, positions=None):
+        s = np.asarray(s, np.float64)
+        pos = np.arange(len(s)) if positions is None else np.asarray(positions)
+        order = np.lexsort((-pos, -s))
+        out = np.full(k, -1)
+        ch = np.sort(pos[order[:k]])
+        out[:len(ch)] = ch
+        return out
+    _fails(P.check_topk, ties_high)
+
+    def descending(s, k, positions=None):
+        out = csa2.topk_positions(s, k, positions)
+        v = out[out >= 0][::-1]
+        return np.concatenate([v, out[out < 0]])
+    _fails(P.check_topk, descending)
+
+
+def test_attention_missing_scale_or_transposed_softmax_is_caught():
+    _fails(P.check_attention, lambda q, v, scale=None: csa2.sparse_attention(q, v, 1.0))
+
+    def wrong_axis(q, v, scale=None):
+        logits = (np.asarray(q) @ np.asarray(v).T) / math.sqrt(512)
+        p = np.exp(logits - logits.max(0, keepdims=True))
+        return (p / p.sum(0, keepdims=True)) @ v
+    _fails(P.check_attention, wrong_axis)
+
+
+def test_hsi_rescoring_with_the_wrong_indexer_is_caught():
+    def bad(keys, q1, w1, q2, w2, pool=16384, k=512):
+        return csa2.hsi_select(keys, q1, w1, q1, w1, pool, k)
+    _fails(P.check_hsi, bad, csa2.indexer_scores, csa2.topk_positions)
