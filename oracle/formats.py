@@ -60,7 +60,7 @@ def e2m1_encode(v) -> np.ndarray:
     v = np.asarray(v, dtype=np.float64)
     if not np.all(np.isfinite(v)):
         raise ValueError("E2M1 encode: non-finite input")
-    a = np.abs(v)
+    a = np.minimum(np.abs(v), 6.0)                        # satfinite: clamp, then round
     d = np.abs(a[..., None] - E2M1_MAGNITUDES)          # distance to each magnitude
     dmin = d.min(axis=-1, keepdims=True)
     nearest = d == dmin                                   # one or two candidates

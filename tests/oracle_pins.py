@@ -88,7 +88,7 @@ def e4m3_brute(v: Fraction) -> int:
 def e2m1_test_values():
     """Tie points, their float32 neighbours, the grid itself, and random values."""
     ties = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
-    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, 7.0, 100.0]
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, 7.0, 100.0, 1e30, 3.0e38]
     vals = []
     for t in ties + grid:
         t32 = np.float32(t)
