@@ -1,0 +1,182 @@
+"""CSA2 FP4 compressed-KV decode path on B300 (sm_103a).
+
+Thin torch-facing binding of the C ABI in ``include/csa2.h`` (libcsa2.so). Every
+function here only marshals arguments (device pointers, sizes, the current CUDA
+stream) and calls the library of the same name; all computation runs in the
+library's CUDA kernels. torch provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+
+import torch
+
+from . import _abi as A
+from ._abi import Csa2Error, FULL, REINDEX, REUSE  # noqa: F401
+
+LATENT_DIM, INDEXER_DIM, INDEXER_HEADS = A.LATENT_DIM, A.INDEXER_DIM, A.INDEXER_HEADS
+DEFAULT_SCALE = 1.0 / math.sqrt(LATENT_DIM)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return A.F32
+    if t.dtype == torch.bfloat16:
+        return A.BF16
+    raise TypeError(f"expected float32 or bfloat16, got {t.dtype}")
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+class Cache:
+    """One layer's global cache: SoA device arrays (see include/csa2.h).
+
+    lat_codes [B, cap, 256] u8, lat_scales [B, cap, 32] u8, idx_codes [B, cap, 64] u8,
+    idx_scales [B, cap, 4] u8, len [B] int32. ``cap`` is a multiple of 128.
+    """
+
+    def __init__(self, batch: int, cap: int, device="cuda"):
+        if cap % 128:
+            raise ValueError("cap must be a multiple of 128")
+        self.batch, self.cap = batch, cap
+        u8 = dict(dtype=torch.uint8, device=device)
+        self.lat_codes = torch.zeros(batch, cap, 256, **u8)
+        self.lat_scales = torch.zeros(batch, cap, 32, **u8)
+        self.idx_codes = torch.zeros(batch, cap, 64, **u8)
+        self.idx_scales = torch.zeros(batch, cap, 4, **u8)
+        self.len = torch.zeros(batch, dtype=torch.int32, device=device)
+        self._view = None
+
+    def view(self) -> A.CacheView:
+        if self._view is None:
+            self._view = A.CacheView(self.lat_codes.data_ptr(), self.lat_scales.data_ptr(),
+                                     self.idx_codes.data_ptr(), self.idx_scales.data_ptr(),
+                                     self.len.data_ptr(), self.cap, self.batch)
+        return self._view
+
+
+def kv_quant_append(lat, ikey, ratio: int, cache: Cache, w0_lat=None, w1_lat=None, w0_idx=None, w1_idx=None,
+                    stream=None) -> None:
+    """Append T tokens per sequence (lat [B,T,512], ikey [B,T,128]; f32 or bf16)."""
+    _contig(lat, ikey, w0_lat, w1_lat, w0_idx, w1_idx)
+    A.check(A.lib().kv_quant_append(_ptr(lat), _ptr(ikey), _dt(lat), lat.shape[1], ratio, _ptr(w0_lat),
+                                    _ptr(w1_lat), _ptr(w0_idx), _ptr(w1_idx), C.byref(cache.view()),
+                                    _stream(stream)), "kv_quant_append")
+
+
+def indexer_score(q_idx, w, idx_codes, idx_scales, length, scores=None, cand=None, stream=None):
+    """scores [B, cap] (or [B, P] with cand [B, P]) of the 4-head indexer."""
+    _contig(q_idx, w, idx_codes, idx_scales, length, cand)
+    B, cap = idx_codes.shape[0], idx_codes.shape[1]
+    P = 0 if cand is None else cand.shape[1]
+    if scores is None:
+        scores = torch.empty(B, P if cand is not None else cap, dtype=torch.float32, device=idx_codes.device)
+    A.check(A.lib().indexer_score(_ptr(q_idx), _dt(q_idx), _ptr(w), _ptr(idx_codes), _ptr(idx_scales), cap,
+                                  _ptr(length), _ptr(cand), P, _ptr(scores), B, _stream(stream)), "indexer_score")
+    return scores
+
+
+def topk_select(scores, k: int, n=None, out=None, cand=None, stream=None):
+    """Exact Top-k positions per row, ascending, -1 padded: out [B, k] int32."""
+    _contig(scores, n, cand)
+    B, stride = scores.shape
+    if out is None:
+        out = torch.empty(B, k, dtype=torch.int32, device=scores.device)
+    A.check(A.lib().topk_select(_ptr(scores), _ptr(n), stride, k, _ptr(cand), _ptr(out), B, None, 0,
+                                _stream(stream)), "topk_select")
+    return out
+
+
+def attn_workspace_size(batch: int, H: int, k: int, W: int = 0) -> int:
+    return A.lib().csa2_attn_workspace_size(batch, H, k, W)
+
+
+def sparse_latent_attn(q, cache: Cache, idx, out=None, swa=None, scale: float = DEFAULT_SCALE, ws=None,
+                       stream=None):
+    """o [B, H, 512] f32 from q [B, H, 512], selected positions idx [B, k], window swa [B, W, 512] bf16."""
+    _contig(q, idx, swa, out)
+    B, H, _ = q.shape
+    k = 0 if idx is None else idx.shape[1]
+    W = 0 if swa is None else swa.shape[1]
+    if out is None:
+        out = torch.empty(B, H, LATENT_DIM, dtype=torch.float32, device=q.device)
+    need = attn_workspace_size(B, H, k, W)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    A.check(A.lib().sparse_latent_attn(_ptr(q), _dt(q), H, scale, C.byref(cache.view()), _ptr(idx), k, _ptr(swa),
+                                       W, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "sparse_latent_attn")
+    return out
+
+
+class Layer:
+    """One layer of a decode step (fields as in csa2_layer_desc)."""
+
+    def __init__(self, mode, q, out, cache: Cache | None = None, q_idx=None, w_idx=None, own_idx_codes=None,
+                 own_idx_scales=None, pool: int = 0, q_idx2=None, w_idx2=None, swa=None, idx_out=None):
+        self.mode, self.q, self.out, self.cache = mode, q, out, cache
+        self.q_idx, self.w_idx = q_idx, w_idx
+        self.own_idx_codes, self.own_idx_scales = own_idx_codes, own_idx_scales
+        self.pool, self.q_idx2, self.w_idx2, self.swa = pool, q_idx2, w_idx2, swa
+        self.idx_out = idx_out
+
+    def desc(self) -> A.LayerDesc:
+        _contig(self.q, self.out, self.q_idx, self.w_idx, self.q_idx2, self.w_idx2, self.swa)
+        cache_ptr = C.pointer(self.cache.view()) if self.cache is not None else None
+        return A.LayerDesc(self.mode, cache_ptr, _ptr(self.own_idx_codes), _ptr(self.own_idx_scales),
+                           _ptr(self.q_idx), _ptr(self.w_idx), self.pool, _ptr(self.q_idx2), _ptr(self.w_idx2),
+                           _ptr(self.q), _ptr(self.swa), 0 if self.swa is None else self.swa.shape[1],
+                           _ptr(self.out), _ptr(self.idx_out))
+
+
+def workspace_size(batch: int, max_entries: int, H: int, k: int = 512, pool: int = 0, W: int = 0) -> int:
+    return A.lib().csa2_workspace_size(batch, max_entries, H, k, pool, W)
+
+
+class DecodeStep:
+    """A prepared decode step: the layer descriptors are built once, each call only launches."""
+
+    def __init__(self, layers, k: int = 512, ws=None):
+        self.layers = list(layers)
+        self.k = k
+        first = self.layers[0]
+        B, H = first.q.shape[0], first.q.shape[1]
+        self.B, self.H, self.dtype = B, H, _dt(first.q)
+        cap = max(L.cache.cap for L in self.layers if L.cache is not None)
+        pool = max(L.pool for L in self.layers)
+        W = max(0 if L.swa is None else L.swa.shape[1] for L in self.layers)
+        need = workspace_size(B, cap, H, k, pool, W)
+        self.ws = ws if ws is not None and ws.numel() >= need else torch.empty(need, dtype=torch.uint8,
+                                                                               device=first.q.device)
+        self._descs = (A.LayerDesc * len(self.layers))(*[L.desc() for L in self.layers])
+
+    def __call__(self, stream=None) -> None:
+        A.check(A.lib().csa2_decode_step(self._descs, len(self.layers), self.B, self.H, self.k, self.dtype,
+                                         _ptr(self.ws), self.ws.numel(), _stream(stream)), "csa2_decode_step")
+
+
+def csa2_decode_step(layers, k: int = 512, ws=None, stream=None) -> None:
+    """Run one decode step through ``layers`` (a list of Layer)."""
+    DecodeStep(layers, k, ws)(stream)
+
+
+def sync_status(stream=None) -> int:
+    """Synchronise and return (and clear) the device status word; 0 = no device error."""
+    return A.lib().csa2_sync_status(_stream(stream))
+
+
+def launch_count() -> int:
+    return A.lib().csa2_launch_count()

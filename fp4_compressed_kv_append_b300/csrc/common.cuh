@@ -1,0 +1,130 @@
+// Device helpers shared by the CSA2 kernels: the device status word, FP4/FP8
+// scalar conversions written from the format definitions, and small PTX wrappers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_fp4.h>
+
+#include "csa2.h"
+
+namespace csa2 {
+
+// First device-side error of the process (0 = none); read and cleared by
+// csa2_sync_status().
+__device__ int g_dev_error = 0;
+
+__device__ __forceinline__ void set_dev_error(int code) { atomicCAS(&g_dev_error, 0, code); }
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// Eight consecutive source values (f32 or bf16) as float; p is 16-byte aligned.
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&x)[8]);
+
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&x)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+template <>
+__device__ __forceinline__ void load8<uint16_t>(const uint16_t* p, float (&x)[8]) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void load4(const T* p, float (&x)[4]);
+
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&x)[4]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+}
+
+template <>
+__device__ __forceinline__ void load4<uint16_t>(const uint16_t* p, float (&x)[4]) {
+  const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
+  x[0] = __uint_as_float(a.x << 16);
+  x[1] = __uint_as_float(a.x & 0xFFFF0000u);
+  x[2] = __uint_as_float(a.y << 16);
+  x[3] = __uint_as_float(a.y & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ float load_elem(const void* p, int dtype, size_t i) {
+  return dtype == CSA2_F32 ? __ldg(static_cast<const float*>(p) + i)
+                           : bf16_bits_to_float(__ldg(static_cast<const uint16_t*>(p) + i));
+}
+
+// ---------------------------------------------------------------- E2M1 (FP4)
+// Round |v| to the nearest E2M1 magnitude, ties to the even mantissa bit,
+// saturating at 6; the sign bit of v becomes bit 3 (a small negative value
+// encodes as 0x8). Magnitudes by code: 0, 0.5, 1, 1.5, 2, 3, 4, 6. The tie
+// points between neighbours are 0.25, 0.75, 1.25, 1.75, 2.5, 3.5 and 5; a tie
+// goes up exactly when the upper neighbour has an even code.
+__device__ __forceinline__ uint32_t e2m1_encode(float v) {
+  const float a = fabsf(v);
+  uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+               (a >= 3.5f) + (a > 5.0f);
+  return m | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// E2M1 magnitude of a 3-bit code (exponent bias 1; exponent 0 is subnormal).
+__device__ __forceinline__ float e2m1_magnitude(uint32_t c3) {
+  const uint32_t e = c3 >> 1, m = c3 & 1u;
+  return e == 0 ? 0.5f * (float)m : __uint_as_float(((e - 1u + 127u) << 23) | (m << 22));
+}
+
+// ---------------------------------------------------------------- E4M3 / E8M0
+// float8_e4m3fn code -> float (finite codes; exponent bias 7, subnormals m/8*2^-6).
+__device__ __forceinline__ float e4m3_decode(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  const float mag = e == 0 ? (float)m * 0.001953125f /* 2^-9 */
+                           : __uint_as_float(((e - 7u + 127u) << 23) | (m << 20));
+  return (c & 0x80u) ? -mag : mag;
+}
+
+// Nearest E4M3 value (ties to even), saturating to the largest finite value.
+__device__ __forceinline__ uint32_t e4m3_encode_satfinite(float v) {
+  return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// 2^(e-127) for an E8M0 byte (e < 255), including the subnormal 2^-127.
+__device__ __forceinline__ float e8m0_decode(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+// ---------------------------------------------------------------- ordered keys
+// Monotone map of a float to uint32 (larger float -> larger key); -0 equals +0.
+__device__ __forceinline__ uint32_t float_order_key(float s) {
+  uint32_t u = __float_as_uint(s);
+  if (u == 0x80000000u) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------- misc
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace csa2

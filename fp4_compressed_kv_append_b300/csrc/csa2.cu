@@ -1,0 +1,325 @@
+// libcsa2: host side of the C ABI declared in include/csa2.h. Validates
+// arguments, sizes grids and launches the kernels of this directory on the
+// caller's stream. The library allocates no device memory.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+#include "quant_append.cuh"
+#include "indexer_scan.cuh"
+#include "topk.cuh"
+#include "attention.cuh"
+
+namespace csa2 {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline csa2_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+}
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+csa2_status check_cache(const csa2_cache_view* c) {
+  if (!c || !c->lat_codes || !c->lat_scales || !c->idx_codes || !c->idx_scales || !c->len)
+    return CSA2_ERR_ARG;
+  if (c->cap <= 0 || (c->cap % 128) != 0 || c->batch <= 0 || c->batch > 65535) return CSA2_ERR_ARG;
+  if (c->cap > (int64_t)INT32_MAX) return CSA2_ERR_UNSUPPORTED;
+  if (!aligned16(c->lat_codes) || !aligned16(c->lat_scales) || !aligned16(c->idx_codes) ||
+      !aligned16(c->idx_scales))
+    return CSA2_ERR_ALIGN;
+  return CSA2_OK;
+}
+
+inline int attn_splits(int k, int W) { return (k + kAttnKeys - 1) / kAttnKeys + (W + kAttnKeys - 1) / kAttnKeys; }
+
+size_t attn_ws_bytes(int batch, int H, int k, int W) {
+  const size_t s = (size_t)attn_splits(k, W);
+  return round_up(s * batch * H * 512 * sizeof(float), 256) + round_up(s * batch * H * 2 * sizeof(float), 256);
+}
+
+// ------------------------------------------------------------ launchers (no validation)
+void launch_append(const void* lat, const void* ikey, csa2_dtype dt, int T, int ratio, const float* w0l,
+                   const float* w1l, const float* w0i, const float* w1i, const csa2_cache_view& c,
+                   cudaStream_t s) {
+  const int n_new = T / ratio;
+  const dim3 grid((n_new + kAppendWarps - 1) / kAppendWarps, c.batch);
+  if (dt == CSA2_F32)
+    k_quant_append<float><<<grid, kAppendWarps * 32, 0, s>>>(
+        (const float*)lat, (const float*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes, c.lat_scales,
+        c.idx_codes, c.idx_scales, c.len, c.cap, n_new);
+  else
+    k_quant_append<uint16_t><<<grid, kAppendWarps * 32, 0, s>>>(
+        (const uint16_t*)lat, (const uint16_t*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes,
+        c.lat_scales, c.idx_codes, c.idx_scales, c.len, c.cap, n_new);
+  k_bump_len<<<(c.batch + 255) / 256, 256, 0, s>>>(c.len, c.batch, c.cap, n_new);
+  g_launches += 2;
+}
+
+void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
+                 int64_t cap, const int32_t* len, const int32_t* cand, int P, float* scores, int batch,
+                 cudaStream_t s) {
+  const int64_t n = cand ? P : cap;
+  const int64_t stride = cand ? P : cap;
+  const dim3 grid((unsigned)((n + kScanThreads - 1) / kScanThreads), batch);
+  k_indexer_scan_simple<<<grid, kScanThreads, 0, s>>>(q_idx, (int)dt, w, codes, scales, cap, len, cand, P,
+                                                       scores, stride);
+  g_launches += 1;
+}
+
+void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,
+                 int32_t* out, int batch, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TopkShared));
+    attr_set = true;
+  }
+  k_topk<<<batch, kTopkThreads, sizeof(TopkShared), s>>>(scores, stride, n, cand, k, out);
+  g_launches += 1;
+}
+
+template <int HT>
+void launch_attn_t(const void* q, csa2_dtype dt, float scale, const csa2_cache_view& c, const int32_t* idx, int k,
+                   const uint16_t* swa, int W, int n_idx_splits, int n_splits, float* part_o, float* part_ml,
+                   cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(k_sparse_attn_mma<HT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)AttnShape<HT>::smem);
+    attr_set = true;
+  }
+  k_sparse_attn_mma<HT><<<dim3(n_splits, c.batch), kAttnThreads, AttnShape<HT>::smem, s>>>(
+      q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, n_idx_splits, part_o,
+      part_ml);
+}
+
+void launch_attn(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
+                 int k, const uint16_t* swa, int W, float* out, void* ws, cudaStream_t s) {
+  const int n_idx_splits = (k + kAttnKeys - 1) / kAttnKeys;
+  const int n_splits = attn_splits(k, W);
+  const size_t s_count = (size_t)n_splits;
+  float* part_o = static_cast<float*>(ws);
+  float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                            round_up(s_count * c.batch * H * 512 * sizeof(float), 256));
+  if (n_splits > 0) {
+    if (H == 16) launch_attn_t<1>(q, dt, scale, c, idx, k, swa, W, n_idx_splits, n_splits, part_o, part_ml, s);
+    else if (H == 32) launch_attn_t<2>(q, dt, scale, c, idx, k, swa, W, n_idx_splits, n_splits, part_o, part_ml, s);
+    else launch_attn_t<4>(q, dt, scale, c, idx, k, swa, W, n_idx_splits, n_splits, part_o, part_ml, s);
+    g_launches += 1;
+  }
+  k_attn_combine<<<dim3(H, c.batch), 128, 0, s>>>(part_o, part_ml, n_splits, H, out);
+  g_launches += 1;
+}
+
+}  // namespace
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" {
+
+csa2_status kv_quant_append(const void* lat, const void* ikey, csa2_dtype in_dtype, int32_t T, int32_t ratio,
+                            const float* w0_lat, const float* w1_lat, const float* w0_idx, const float* w1_idx,
+                            const csa2_cache_view* cache, csa2_stream_t stream) {
+  const csa2_status cs = check_cache(cache);
+  if (cs != CSA2_OK) return cs;
+  if (in_dtype != CSA2_F32 && in_dtype != CSA2_BF16) return CSA2_ERR_ARG;
+  if (T < 0 || (ratio != 1 && ratio != 2)) return CSA2_ERR_ARG;
+  if (ratio == 2 && ((T & 1) || !w0_lat || !w1_lat || !w0_idx || !w1_idx)) return CSA2_ERR_ARG;
+  if (T == 0) return CSA2_OK;
+  if (!lat || !ikey) return CSA2_ERR_ARG;
+  if (!aligned16(lat) || !aligned16(ikey)) return CSA2_ERR_ALIGN;
+  launch_append(lat, ikey, in_dtype, T, ratio, w0_lat, w1_lat, w0_idx, w1_idx, *cache, (cudaStream_t)stream);
+  return launch_status();
+}
+
+csa2_status indexer_score(const void* q_idx, csa2_dtype q_dtype, const float* w, const uint8_t* idx_codes,
+                          const uint8_t* idx_scales, int64_t cap, const int32_t* len, const int32_t* cand,
+                          int32_t P, float* scores, int32_t batch, csa2_stream_t stream) {
+  if (!q_idx || !w || !idx_codes || !idx_scales || !len || !scores) return CSA2_ERR_ARG;
+  if (q_dtype != CSA2_F32 && q_dtype != CSA2_BF16) return CSA2_ERR_ARG;
+  if (cap <= 0 || cap % 128 || cap > INT32_MAX || batch <= 0 || batch > 65535) return CSA2_ERR_ARG;
+  if (cand && (P <= 0 || P > CSA2_MAX_TOPK)) return CSA2_ERR_ARG;
+  if (!aligned16(idx_codes) || !aligned16(idx_scales)) return CSA2_ERR_ALIGN;
+  launch_scan(q_idx, q_dtype, w, idx_codes, idx_scales, cap, len, cand, P, scores, batch, (cudaStream_t)stream);
+  return launch_status();
+}
+
+csa2_status topk_select(const float* scores, const int32_t* n, int64_t stride, int32_t k, const int32_t* cand,
+                        int32_t* out_idx, int32_t batch, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (!scores || !out_idx) return CSA2_ERR_ARG;
+  if (stride <= 0 || stride > INT32_MAX || k < 1 || k > CSA2_MAX_TOPK || batch <= 0) return CSA2_ERR_ARG;
+  launch_topk(scores, n, stride, k, cand, out_idx, batch, (cudaStream_t)stream);
+  return launch_status();
+}
+
+csa2_status sparse_latent_attn(const void* q, csa2_dtype q_dtype, int32_t H, float scale,
+                               const csa2_cache_view* cache, const int32_t* idx, int32_t k, const uint16_t* swa,
+                               int32_t W, float* out, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  const csa2_status cs = check_cache(cache);
+  if (cs != CSA2_OK) return cs;
+  if (!q || !out || (q_dtype != CSA2_F32 && q_dtype != CSA2_BF16)) return CSA2_ERR_ARG;
+  if (H != 16 && H != 32 && H != 64) return CSA2_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || k < 0 || k > CSA2_MAX_TOPK || W < 0 || W > CSA2_MAX_WINDOW) return CSA2_ERR_ARG;
+  if ((k > 0 && !idx) || (W > 0 && !swa)) return CSA2_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out) || (W > 0 && !aligned16(swa))) return CSA2_ERR_ALIGN;
+  if (!ws || ws_bytes < attn_ws_bytes(cache->batch, H, k, W)) return CSA2_ERR_WORKSPACE;
+  if (!aligned16(ws)) return CSA2_ERR_ALIGN;
+  launch_attn(q, q_dtype, H, scale, *cache, idx, k, swa, W, out, ws, (cudaStream_t)stream);
+  return launch_status();
+}
+
+size_t csa2_attn_workspace_size(int32_t batch, int32_t H, int32_t k, int32_t W) {
+  return attn_ws_bytes(batch, H, k, W);
+}
+
+size_t csa2_topk_workspace_size(int32_t batch, int64_t stride, int32_t k) {
+  (void)batch;
+  (void)stride;
+  (void)k;
+  return 0;
+}
+
+namespace {
+struct StepLayout {
+  size_t scores, pool, pscores, sel, attn, total;
+};
+
+StepLayout step_layout(int32_t batch, int64_t max_entries, int32_t H, int32_t k, int32_t pool, int32_t W) {
+  StepLayout L{};
+  size_t off = 0;
+  L.scores = off;
+  off += round_up((size_t)batch * (size_t)max_entries * sizeof(float), 256);
+  L.pool = off;
+  off += round_up((size_t)batch * (size_t)pool * sizeof(int32_t), 256);
+  L.pscores = off;
+  off += round_up((size_t)batch * (size_t)pool * sizeof(float), 256);
+  L.sel = off;
+  off += round_up((size_t)batch * (size_t)k * sizeof(int32_t), 256);
+  L.attn = off;
+  off += attn_ws_bytes(batch, H, k, W);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+size_t csa2_workspace_size(int32_t batch, int64_t max_entries, int32_t H, int32_t k, int32_t pool, int32_t W) {
+  return step_layout(batch, max_entries, H, k, pool, W).total;
+}
+
+csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, int32_t batch, int32_t H, int32_t k,
+                             csa2_dtype dtype, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  if (!layers || n_layers < 1 || batch <= 0 || batch > 65535) return CSA2_ERR_ARG;
+  if (dtype != CSA2_F32 && dtype != CSA2_BF16) return CSA2_ERR_ARG;
+  if (H != 16 && H != 32 && H != 64) return CSA2_ERR_UNSUPPORTED;
+  if (k < 1 || k > CSA2_MAX_TOPK) return CSA2_ERR_ARG;
+  if (layers[0].mode != CSA2_FULL) return CSA2_ERR_ARG;
+  // validate every layer and find the workspace sizes
+  int64_t max_cap = 0;
+  int32_t max_pool = 0, max_W = 0;
+  for (int i = 0; i < n_layers; ++i) {
+    const csa2_layer_desc& L = layers[i];
+    if (L.mode != CSA2_FULL && L.mode != CSA2_REINDEX && L.mode != CSA2_REUSE) return CSA2_ERR_ARG;
+    if (!L.q || !L.out || L.W < 0 || L.W > CSA2_MAX_WINDOW || (L.W > 0 && !L.swa)) return CSA2_ERR_ARG;
+    if (!aligned16(L.q) || !aligned16(L.out) || (L.W > 0 && !aligned16(L.swa))) return CSA2_ERR_ALIGN;
+    if (L.mode == CSA2_FULL) {
+      const csa2_status cs = check_cache(L.cache);
+      if (cs != CSA2_OK) return cs;
+      if (L.cache->batch != batch) return CSA2_ERR_ARG;
+      if (L.pool < 0 || L.pool > CSA2_MAX_TOPK || (L.pool > 0 && (L.pool <= k || !L.q_idx2 || !L.w_idx2)))
+        return CSA2_ERR_ARG;
+      max_cap = L.cache->cap > max_cap ? L.cache->cap : max_cap;
+      max_pool = L.pool > max_pool ? L.pool : max_pool;
+    }
+    if (L.mode != CSA2_REUSE && (!L.q_idx || !L.w_idx)) return CSA2_ERR_ARG;
+    if (L.mode == CSA2_REINDEX && ((L.own_idx_codes == nullptr) != (L.own_idx_scales == nullptr)))
+      return CSA2_ERR_ARG;
+    if (L.mode == CSA2_REINDEX && L.own_idx_codes && (!aligned16(L.own_idx_codes) || !aligned16(L.own_idx_scales)))
+      return CSA2_ERR_ALIGN;
+    max_W = L.W > max_W ? L.W : max_W;
+  }
+  const StepLayout SL = step_layout(batch, max_cap, H, k, max_pool, max_W);
+  if (!ws || ws_bytes < SL.total) return CSA2_ERR_WORKSPACE;
+  if (!aligned16(ws)) return CSA2_ERR_ALIGN;
+  char* base = static_cast<char*>(ws);
+  float* scores = reinterpret_cast<float*>(base + SL.scores);
+  int32_t* pool_idx = reinterpret_cast<int32_t*>(base + SL.pool);
+  float* pscores = reinterpret_cast<float*>(base + SL.pscores);
+  int32_t* sel = reinterpret_cast<int32_t*>(base + SL.sel);
+  void* attn_ws = base + SL.attn;
+  cudaStream_t s = (cudaStream_t)stream;
+
+  const csa2_cache_view* main = nullptr;
+  const int32_t* last = nullptr;
+  int pool = 0;
+  for (int i = 0; i < n_layers; ++i) {
+    const csa2_layer_desc& L = layers[i];
+    int32_t* dst = L.idx_out ? L.idx_out : sel;
+    if (L.mode == CSA2_FULL) {
+      main = L.cache;
+      pool = L.pool;
+      launch_scan(L.q_idx, dtype, L.w_idx, main->idx_codes, main->idx_scales, main->cap, main->len, nullptr, 0,
+                  scores, batch, s);
+      if (pool > 0) {
+        launch_topk(scores, main->len, main->cap, pool, nullptr, pool_idx, batch, s);
+        launch_scan(L.q_idx2, dtype, L.w_idx2, main->idx_codes, main->idx_scales, main->cap, main->len, pool_idx,
+                    pool, pscores, batch, s);
+        launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s);
+      } else {
+        launch_topk(scores, main->len, main->cap, k, nullptr, dst, batch, s);
+      }
+      last = dst;
+    } else if (L.mode == CSA2_REINDEX) {
+      const uint8_t* kc = L.own_idx_codes ? L.own_idx_codes : main->idx_codes;
+      const uint8_t* ksc = L.own_idx_scales ? L.own_idx_scales : main->idx_scales;
+      if (pool > 0) {
+        launch_scan(L.q_idx, dtype, L.w_idx, kc, ksc, main->cap, main->len, pool_idx, pool, pscores, batch, s);
+        launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s);
+      } else {
+        launch_scan(L.q_idx, dtype, L.w_idx, kc, ksc, main->cap, main->len, nullptr, 0, scores, batch, s);
+        launch_topk(scores, main->len, main->cap, k, nullptr, dst, batch, s);
+      }
+      last = dst;
+    } else if (L.idx_out) {
+      if (cudaMemcpyAsync(L.idx_out, last, (size_t)batch * k * sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
+          cudaSuccess)
+        return CSA2_ERR_CUDA;
+    }
+    launch_attn(L.q, dtype, H, 1.0f / sqrtf((float)CSA2_LATENT_DIM), *main, last, k, L.swa, L.W, L.out, attn_ws, s);
+  }
+  return launch_status();
+}
+
+csa2_status csa2_sync_status(csa2_stream_t stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CSA2_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof(int)) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(int)) != cudaSuccess) return CSA2_ERR_CUDA;
+  }
+  return (csa2_status)v;
+}
+
+const char* csa2_status_str(csa2_status st) {
+  switch (st) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_ARG: return "invalid argument";
+    case CSA2_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported shape";
+    case CSA2_ERR_CUDA: return "CUDA runtime error";
+    case CSA2_ERR_TIMEOUT: return "device wait timed out";
+    case CSA2_ERR_BOUNDS: return "index or append outside the cache";
+    case CSA2_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+uint64_t csa2_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,125 @@
+"""Whole decode steps of the five workloads against the oracle.
+
+Reduced sizes (several tiles and a ragged tail) are checked on every sequence;
+the full sizes are checked on sampled sequences, plus properties on all of them.
+"""
+import numpy as np
+import pytest
+import torch
+
+from fp4_compressed_kv_append_b300 import configs as CF
+from oracle import csa2 as O
+from tests import harness as Hh
+from tests.harness import np_
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_rows(c, b, stream="tokens"):
+    lat, ikey = CF.source_tokens(c, b, stream=stream)
+    w = [np_(x) for x in CF.WL.merge_weights(c["seed"], device="cuda")] if c["ratio"] == 2 else [None] * 4
+    lat, ikey = np_(lat), np_(ikey)
+    step = 4096 * c["ratio"]
+    parts = [O.encode_entries(lat[i:i + step], ikey[i:i + step], c["ratio"], *w) for i in range(0, len(lat), step)]
+    return tuple(np.concatenate([p[j] for p in parts]) for j in range(4))
+
+
+def _check_sequence(wl: CF.DecodeWorkload, b: int):
+    c = wl.c
+    rows = _oracle_rows(c, b)
+    Hh.assert_rows_equal(wl.cache, b, rows)
+    host = Hh.host_cache_from_rows([rows], wl.cache.cap)
+    own = None
+    if wl.reindex_keys is not None:
+        r2 = _oracle_rows(c, b, stream="reindex-keys")
+        Hh.assert_rows_equal(wl.reindex_keys, b, r2)
+        own = Hh.host_cache_from_rows([r2], wl.cache.cap)
+    f64 = lambda t: None if t is None else np_(t[b:b + 1]).astype(np.float64)  # noqa: E731
+    layers = []
+    for li, mode in enumerate(c["modes"]):
+        inp = wl.inputs[li]
+        L = dict(mode=mode, q=f64(inp["q"]), swa=f64(inp["swa"]))
+        if mode == O.FULL:
+            L.update(cache=host, q_idx=f64(inp["q_idx"]), w_idx=f64(inp["w_idx"]), pool=c["pool"],
+                     q_idx2=f64(inp["q_idx2"]), w_idx2=f64(inp["w_idx2"]))
+        elif mode == O.REINDEX:
+            L.update(q_idx=f64(inp["q_idx"]), w_idx=f64(inp["w_idx"]),
+                     keys_codes=own.idx_codes if own else None, keys_scales=own.idx_scales if own else None)
+        layers.append(L)
+    outs, idxs = O.decode_step(layers, CF.TOPK)
+    n = int(host.len[0])
+    keys_main = O.entry_keys(host.idx_codes[0, :n], host.idx_scales[0, :n])
+    swaps = 0
+    for li, mode in enumerate(c["modes"]):
+        got_idx = np_(wl.indices[li][b])
+        inp = wl.inputs[li]
+        if mode == O.FULL and c["pool"]:
+            s1 = O.indexer_scores(f64(inp["q_idx"])[0], f64(inp["w_idx"])[0], keys_main)
+            pool = O.topk_positions(s1, c["pool"])
+            pv = pool[pool >= 0]
+            s2 = O.indexer_scores(f64(inp["q_idx2"])[0], f64(inp["w_idx2"])[0], keys_main[pv])
+            swaps += Hh.assert_topk_match(got_idx, idxs[li][0], s2, positions=pv, where=f"seq {b} layer {li}")
+        elif mode in (O.FULL, O.REINDEX):
+            keys = keys_main if (mode == O.FULL or own is None) else O.entry_keys(own.idx_codes[0, :n],
+                                                                                  own.idx_scales[0, :n])
+            s = O.indexer_scores(f64(inp["q_idx"])[0], f64(inp["w_idx"])[0], keys)
+            swaps += Hh.assert_topk_match(got_idx, idxs[li][0], s, where=f"seq {b} layer {li}")
+        else:
+            assert np.array_equal(got_idx, np_(wl.indices[li - 1][b]))
+        if np.array_equal(got_idx, idxs[li][0]):
+            err = Hh.attn_rel_err(np_(wl.outputs[li][b]), outs[li][0])
+            assert err <= Hh.ATTN_TOL, (b, li, err)
+    return swaps
+
+
+def _run(cfg_id, sample=None, **override):
+    c = CF.config(cfg_id, **override)
+    wl = CF.DecodeWorkload(c)
+    wl()
+    torch.cuda.synchronize()
+    assert CF.WL is not None and Hh.K.sync_status() == 0
+    B = c["B"]
+    n = int(wl.cache.len[0])
+    for li in range(len(c["modes"])):  # properties on every sequence
+        idx = wl.indices[li].cpu().numpy()
+        for b in range(B):
+            v = idx[b][idx[b] >= 0]
+            assert len(v) == min(CF.TOPK, n) and np.all(np.diff(v) > 0) and v.max() < n
+        assert torch.isfinite(wl.outputs[li]).all()
+    for b in (range(B) if sample is None else sample):
+        _check_sequence(wl, b)
+
+
+def test_config0_tiny_ratio1_full_size():
+    _run(0)
+
+
+def test_config2_reduced():
+    _run(2, B=3, tokens=2600)
+
+
+def test_config3_reduced_hierarchical_pool():
+    _run(3, B=2, tokens=2 * 20000)
+
+
+def test_config4_reduced_group_with_window():
+    _run(4, B=3, tokens=3000)
+
+
+def test_fewer_entries_than_k():
+    _run(2, B=2, tokens=300)
+
+
+@pytest.mark.slow
+def test_config2_full_size_sampled():
+    _run(2, sample=[0, 31])
+
+
+@pytest.mark.slow
+def test_config3_full_size_sampled():
+    _run(3, sample=[7])
+
+
+@pytest.mark.slow
+def test_config4_full_size_sampled():
+    _run(4, sample=[0, 63])

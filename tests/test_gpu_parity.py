@@ -1,0 +1,206 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Every case is seeded and synthetic (fp4_compressed_kv_append_b300.workloads);
+both sides consume the same source values; no expected value comes from the
+CUDA path.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from tests import harness as Hh
+from tests.harness import K, O, WL, np_
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows_chunked(lat, ikey, ratio, w=None, chunk=4096):
+    """Oracle rows of one sequence, in chunks of whole entries (entries are independent)."""
+    step = chunk * ratio
+    parts = [O.encode_entries(lat[i:i + step], ikey[i:i + step], ratio, *(w or [None] * 4))
+             for i in range(0, lat.shape[0], step)]
+    return tuple(np.concatenate([p[j] for p in parts]) for j in range(4))
+
+
+# ============================================================== append
+@pytest.mark.parametrize("T,ratio,kind", [(4096, 1, "lognormal"), (1337, 1, "lognormal"), (2 * 677, 2, "outlier"),
+                                          (2 * 300, 2, "lognormal"), (1, 1, "outlier")])
+def test_append_bit_exact(T, ratio, kind):
+    seed = 0
+    cap = ((T // ratio + 127) // 128) * 128 + 128
+    w = WL.merge_weights(seed, device="cuda") if ratio == 2 else None
+    B = 2
+    cache = K.Cache(B, cap)
+    for b in range(B):
+        lat, ikey = Hh.sources(kind, seed, b, T, "cuda")
+        K.kv_quant_append(lat[None], ikey[None], ratio, Hh.sub_view(cache, b), *(w or [None] * 4))
+        rows = _rows_chunked(np_(lat), np_(ikey), ratio, None if w is None else [np_(x) for x in w])
+        torch.cuda.synchronize()
+        Hh.assert_rows_equal(cache, b, rows)
+    assert K.sync_status() == 0
+
+
+def test_append_full_cache_write_workload():
+    """65,536 bf16 tokens with outlier channels, ratio 2 -> 32,768 entries, bit-exact."""
+    seed, T = 0, 65536
+    w = WL.merge_weights(seed, device="cuda")
+    lat, ikey = WL.outlier_tokens(seed, 0, T, device="cuda")
+    cache = K.Cache(1, 32768)
+    K.kv_quant_append(lat[None], ikey[None], 2, cache, *w)
+    rows = _rows_chunked(np_(lat), np_(ikey), 2, [np_(x) for x in w])
+    torch.cuda.synchronize()
+    Hh.assert_rows_equal(cache, 0, rows)
+
+
+def test_append_in_two_calls_and_edge_values():
+    """Appends land at len; zero, negative-zero, tiny, huge and saturating blocks."""
+    rng = np.random.default_rng(5)
+    lat = (rng.standard_normal((2, 40, 512)) * 3).astype(np.float32)
+    key = (rng.standard_normal((2, 40, 128)) * 3).astype(np.float32)
+    lat[0, 0, :16] = 0.0
+    lat[0, 1, :16] = -0.0
+    lat[0, 2, 16:32] *= 1e-6
+    lat[0, 3, 32:48] *= 1e5
+    lat[0, 4, 48:64] = 3e38
+    key[0, 0, :32] = 0.0
+    key[0, 1, :32] = -0.0
+    key[0, 2, 32:64] = 2.0 ** -140
+    key[0, 3, 64:96] = 3e38
+    cache = K.Cache(2, 128)
+    tl, tk = torch.from_numpy(lat).cuda(), torch.from_numpy(key).cuda()
+    K.kv_quant_append(tl[:, :25].contiguous(), tk[:, :25].contiguous(), 1, cache)
+    K.kv_quant_append(tl[:, 25:].contiguous(), tk[:, 25:].contiguous(), 1, cache)
+    torch.cuda.synchronize()
+    for b in range(2):
+        Hh.assert_rows_equal(cache, b, O.encode_entries(lat[b], key[b], 1))
+
+
+def test_append_past_capacity_is_refused_on_device():
+    cache = K.Cache(1, 128)
+    lat, ikey = WL.lognormal_tokens(0, 0, 100, device="cuda")
+    K.kv_quant_append(lat[None], ikey[None], 1, cache)
+    K.kv_quant_append(lat[None], ikey[None], 1, cache)  # 200 > 128: refused
+    assert K.sync_status() == K.A.ERR_BOUNDS
+    assert int(cache.len[0]) == 100
+    assert K.sync_status() == 0
+
+
+def test_append_argument_errors():
+    cache = K.Cache(1, 128)
+    lat, ikey = WL.lognormal_tokens(0, 0, 3, device="cuda")
+    with pytest.raises(K.Csa2Error) as e:
+        K.kv_quant_append(lat[None], ikey[None], 2, cache, *WL.merge_weights(0, device="cuda"))
+    assert e.value.status == K.A.ERR_ARG
+    with pytest.raises(K.Csa2Error):
+        K.kv_quant_append(lat[None], ikey[None], 3, cache)
+
+
+# ============================================================== indexer scores
+def _small_cache(B, N, seed=1, cap=None):
+    cap = cap or ((N + 127) // 128) * 128
+    cache = Hh.build_gpu_cache("lognormal", seed, B, N, 1, cap)
+    host = Hh.host_cache_from_rows([Hh.oracle_cache_rows("lognormal", seed, b, N, 1) for b in range(B)], cap)
+    return cache, host
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_indexer_scores_within_fp32_bound(dtype):
+    B, N = 3, 2500
+    cache, host = _small_cache(B, N)
+    _, q_idx, w = WL.queries(1, "scan", B, 16, dtype=dtype, device="cuda")
+    scores = K.indexer_score(q_idx, w, cache.idx_codes, cache.idx_scales, cache.len)
+    torch.cuda.synchronize()
+    for b in range(B):
+        keys = O.entry_keys(host.idx_codes[b, :N], host.idx_scales[b, :N])
+        ref = O.indexer_scores(np_(q_idx[b]).astype(np.float64), np_(w[b]), keys)
+        tol = Hh.score_tolerance(np_(q_idx[b]), np_(w[b]), keys)
+        err = np.abs(np_(scores[b, :N]).astype(np.float64) - ref)
+        assert np.all(err <= tol), (b, float((err / tol).max()))
+
+
+def test_indexer_scores_on_candidates():
+    B, N, P = 2, 1500, 700
+    cache, host = _small_cache(B, N)
+    _, q_idx, w = WL.queries(2, "scan", B, 16, device="cuda")
+    g = torch.Generator().manual_seed(3)
+    cand = torch.stack([torch.sort(torch.randperm(N, generator=g)[:P - 5]).values for _ in range(B)])
+    cand = torch.cat([cand, -torch.ones(B, 5, dtype=torch.long)], 1).to(torch.int32).cuda()
+    scores = K.indexer_score(q_idx, w, cache.idx_codes, cache.idx_scales, cache.len, cand=cand)
+    torch.cuda.synchronize()
+    for b in range(B):
+        c = np_(cand[b])
+        keys = O.entry_keys(host.idx_codes[b, c[c >= 0]], host.idx_scales[b, c[c >= 0]])
+        ref = O.indexer_scores(np_(q_idx[b]).astype(np.float64), np_(w[b]), keys)
+        tol = Hh.score_tolerance(np_(q_idx[b]), np_(w[b]), keys)
+        got = np_(scores[b])
+        assert np.all(np.abs(got[:P - 5] - ref) <= tol)
+        assert np.all(np.isneginf(got[P - 5:]))
+
+
+# ============================================================== Top-k
+@pytest.mark.parametrize("n,k,ties", [(1, 1, 0), (7, 512, 0), (511, 512, 0), (512, 512, 0), (513, 512, 0),
+                                      (4096, 512, 0), (4096, 512, 7), (131072, 512, 0), (131072, 512, 3000),
+                                      (40000, 16384, 0), (5000, 1, 0), (3000, 600, 1)])
+def test_topk_bit_exact(n, k, ties):
+    B = 3
+    s = WL.scores(n * 7 + k, B, n, device="cpu", ties=ties)
+    s[0, : min(n, 5)] = -0.0                       # negative zeros tie with +0
+    nvec = torch.tensor([n, max(n - 3, 0), n // 2], dtype=torch.int32)
+    out = K.topk_select(s.cuda(), k, n=nvec.cuda())
+    torch.cuda.synchronize()
+    for b in range(B):
+        m = int(nvec[b])
+        ref = O.topk_positions(s[b, :m].numpy().astype(np.float64), k)
+        assert np.array_equal(np_(out[b]), ref), b
+
+
+def test_topk_with_candidates():
+    B, P, k = 2, 16384, 512
+    s = WL.scores(9, B, P, device="cpu", ties=50)
+    g = torch.Generator().manual_seed(4)
+    cand = torch.stack([torch.sort(torch.randperm(100000, generator=g)[:P - 100]).values for _ in range(B)])
+    cand = torch.cat([cand, -torch.ones(B, 100, dtype=torch.long)], 1).to(torch.int32)
+    out = K.topk_select(s.cuda(), k, cand=cand.cuda())
+    torch.cuda.synchronize()
+    for b in range(B):
+        c = cand[b].numpy()
+        ok = c >= 0
+        ref = O.topk_positions(s[b].numpy()[ok].astype(np.float64), k, positions=c[ok])
+        assert np.array_equal(np_(out[b]), ref)
+
+
+# ============================================================== attention
+@pytest.mark.parametrize("H,k,W,dtype", [(16, 512, 0, torch.float32), (64, 512, 0, torch.bfloat16),
+                                         (32, 300, 0, torch.bfloat16), (64, 512, 128, torch.bfloat16),
+                                         (64, 1, 77, torch.bfloat16), (64, 0, 128, torch.bfloat16),
+                                         (16, 129, 5, torch.float32), (64, 0, 0, torch.bfloat16)])
+def test_attention_within_2e3(H, k, W, dtype):
+    B, N = 2, 1200
+    cache, host = _small_cache(B, N, seed=4)
+    q, q_idx, w = WL.queries(4, "attn", B, H, dtype=dtype, device="cuda")
+    idx = np.full((B, k), -1, np.int64)
+    for b in range(B):
+        keys = O.entry_keys(host.idx_codes[b, :N], host.idx_scales[b, :N])
+        if k:
+            idx[b] = O.topk_positions(O.indexer_scores(np_(q_idx[b]).astype(np.float64), np_(w[b]), keys), k)
+    swa = WL.window(4, 0, B, W, device="cuda") if W else None
+    out = K.sparse_latent_attn(q, cache, torch.from_numpy(idx).to(torch.int32).cuda() if k else None, swa=swa)
+    torch.cuda.synchronize()
+    assert K.sync_status() == 0
+    for b in range(B):
+        ref = O.attend(np_(q[b]).astype(np.float64), host.lat_codes[b], host.lat_scales[b], idx[b],
+                       None if swa is None else np_(swa[b]).astype(np.float64))
+        err = Hh.attn_rel_err(np_(out[b]), ref)
+        assert err <= Hh.ATTN_TOL, (b, err)
+
+
+def test_attention_index_past_len_is_flagged():
+    B, N = 1, 300
+    cache, host = _small_cache(B, N, seed=5)
+    q, _, _ = WL.queries(5, "attn", B, 64, device="cuda")
+    idx = torch.arange(512, dtype=torch.int32, device="cuda")[None]
+    K.sparse_latent_attn(q, cache, idx)
+    assert K.sync_status() == K.A.ERR_BOUNDS
+    assert K.sync_status() == 0
