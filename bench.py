@@ -25,7 +25,6 @@ import json
 import os
 import statistics
 import sys
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +41,7 @@ STEPS_PER_GRAPH = 16
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=1024)
+    p.add_argument("--steps", type=int, default=4096)
     p.add_argument("--warmup", type=int, default=32)
     p.add_argument("--config", type=int, default=2)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -76,55 +75,57 @@ def max_over_ranks(x, world):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """NVML samples of SM clock, power and throttle reasons while running."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons while running."""
 
-    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
-               0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
-               0x100: "display_clock_setting"}
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, index, period=0.01):
-        self.samples, self.reasons = [], set()
-        self.period, self._stop = period, threading.Event()
-        self.ok = False
+    def __init__(self, device_index):
+        self.rows, self.err, self.proc, self.id = [], None, None, None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
+            self.id = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
         except Exception as e:  # noqa: BLE001
             self.err = repr(e)
 
-    def _run(self):
-        nv = self.nv
-        while not self._stop.is_set():
-            try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
-                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                for bit, name in self.REASONS.items():
-                    if r & bit:
-                        self.reasons.add(name)
-            except Exception:  # noqa: BLE001
-                pass
-            time.sleep(self.period)
-
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
-            self.t.start()
+        import subprocess
+        import tempfile
+        self.out = tempfile.TemporaryFile(mode="w+")
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.id:
+            cmd += ["-i", self.id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception as e:  # noqa: BLE001
+            self.err = repr(e)
         return self
 
     def __exit__(self, *a):
-        if self.ok:
-            self._stop.set()
-            self.t.join()
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait()
+            self.out.seek(0)
+            for line in self.out:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    self.rows.append(parts)
 
     def summary(self):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": getattr(self, "err", "nvml")}
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err or "no samples"}
+        sm = [v for v in (num(r[0]) for r in self.rows) if v is not None]
+        mx = [v for v in (num(r[1]) for r in self.rows) if v is not None]
+        reasons = sorted({n for r in self.rows for n, v in zip(self.NAMES, r[3:]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows), "sampler": "nvidia-smi -lms 50"}
 
 
 def peaks():
