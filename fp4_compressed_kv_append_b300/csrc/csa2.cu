@@ -59,14 +59,52 @@ void launch_append(const void* lat, const void* ikey, csa2_dtype dt, int T, int 
   g_launches += 2;
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+template <int NPART>
+void launch_scan_t(const ScanArgs& a, cudaStream_t s) {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int occ = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_indexer_scan<NPART>, kScanThreads, 0);
+    per_sm = occ > 0 ? occ : 1;
+  }
+  const int64_t want = (a.total_tiles + kScanWarps - 1) / kScanWarps;  // >= 1 tile per warp
+  const int64_t full = (int64_t)sm_count() * per_sm;
+  const int grid = (int)(want < full ? want : full);
+  k_indexer_scan<NPART><<<grid, kScanThreads, 0, s>>>(a);
+}
+
 void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
                  int64_t cap, const int32_t* len, const int32_t* cand, int P, float* scores, int batch,
                  cudaStream_t s) {
-  const int64_t n = cand ? P : cap;
-  const int64_t stride = cand ? P : cap;
-  const dim3 grid((unsigned)((n + kScanThreads - 1) / kScanThreads), batch);
-  k_indexer_scan_simple<<<grid, kScanThreads, 0, s>>>(q_idx, (int)dt, w, codes, scales, cap, len, cand, P,
-                                                       scores, stride);
+  ScanArgs a;
+  a.q_idx = q_idx;
+  a.q_dtype = (int)dt;
+  a.w = w;
+  a.codes = codes;
+  a.scales = scales;
+  a.cap = cap;
+  a.len = len;
+  a.cand = cand;
+  a.P = P;
+  a.scores = scores;
+  a.stride = cand ? P : cap;
+  a.tiles_per_seq = (a.stride + kScanTile - 1) / kScanTile;
+  a.total_tiles = a.tiles_per_seq * batch;
+  if (dt == CSA2_F32) launch_scan_t<2>(a, s);
+  else launch_scan_t<1>(a, s);
   g_launches += 1;
 }
 
@@ -74,10 +112,12 @@ void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, c
                  int32_t* out, int batch, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TopkShared));
+    cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)(sizeof(TopkCtl) + 8u * topk_cap(CSA2_MAX_TOPK)));
     attr_set = true;
   }
-  k_topk<<<batch, kTopkThreads, sizeof(TopkShared), s>>>(scores, stride, n, cand, k, out);
+  const size_t smem = sizeof(TopkCtl) + 8u * topk_cap(k);
+  k_topk<<<batch, kTopkThreads, smem, s>>>(scores, stride, n, cand, k, out);
   g_launches += 1;
 }
 

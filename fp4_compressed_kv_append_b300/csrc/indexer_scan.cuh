@@ -5,71 +5,277 @@
 // indexer key scores positions) and section "Cles d'indexeur" (eq. 68: E2M1 with an
 // E8M0 scale per 32 channels).
 //
-// CUDA-core form: one thread per entry. The 64 code bytes of an entry are read as
-// four 16-byte vectors, the queries live in shared memory as float. Each block of
-// 32 channels is summed unscaled (the codes are exact small numbers), then scaled by
-// its power of two, in float32.
+// The scan reads 68 bytes per entry and does 4 x 128 multiply-adds on them, more
+// arithmetic per byte than the CUDA cores can sustain at HBM speed, so the
+// contraction runs on the tensor cores (mma.sync m16n8k16, fp16 operands, fp32
+// accumulation) and the CUDA cores only unpack codes and finish the epilogue.
+//
+//  * Operand A (16 entries x 16 channels): unscaled E2M1 values, converted from
+//    the packed codes with cvt.rn.f16x2.e2m1x2 -- exact in fp16.
+//  * Operand B (16 channels x 8 columns): the queries, scaled per head by a power
+//    of two 2^s_h so that fp16 keeps every bit of a bf16 query (fp32 queries are
+//    split into fp16 hi + lo parts, a second n-tile). Column n = 4*jj + h holds
+//    head h restricted to block jj of a pair of 32-channel blocks (zero
+//    elsewhere), so one MMA keeps two E8M0 blocks apart and every column is used.
+//  * Epilogue: per block, multiply by its exact power-of-two scale, add the four
+//    blocks, undo 2^s_h inside the head weight, ReLU, weighted head sum.
+//
+// Lane (g = lane/4, t4 = lane%4) of a warp loads, for entries g + 8r (r = 0..3),
+// the 32-bit word t4 of each 16-byte block of codes -- so a k-step's channels
+// (8 t4 + 2 kq + {0,1} of a block) sit in the right fragment slots without any
+// shuffle. Each warp walks a contiguous range of 32-entry tiles (two m16 row
+// tiles), prefetching the next tile's registers while it computes the current one.
 #pragma once
 
 #include "common.cuh"
 
 namespace csa2 {
 
-constexpr int kScanThreads = 256;
+constexpr int kScanWarps = 8;
+constexpr int kScanThreads = kScanWarps * 32;
+constexpr int kScanTile = 32;  // entries per warp iteration
 
-__global__ void __launch_bounds__(kScanThreads)
-k_indexer_scan_simple(const void* __restrict__ q_idx, int q_dtype, const float* __restrict__ w,
-                      const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                      int64_t cap, const int32_t* __restrict__ len,
-                      const int32_t* __restrict__ cand, int P, float* __restrict__ scores,
-                      int64_t stride) {
-  __shared__ float qs[CSA2_INDEXER_HEADS][CSA2_INDEXER_DIM];
-  __shared__ float ws[CSA2_INDEXER_HEADS];
-  const int b = blockIdx.y;
-  for (int i = threadIdx.x; i < CSA2_INDEXER_HEADS * CSA2_INDEXER_DIM; i += blockDim.x)
-    qs[i / CSA2_INDEXER_DIM][i % CSA2_INDEXER_DIM] =
-        load_elem(q_idx, q_dtype, (size_t)b * CSA2_INDEXER_HEADS * CSA2_INDEXER_DIM + i);
-  if (threadIdx.x < CSA2_INDEXER_HEADS) ws[threadIdx.x] = w[b * CSA2_INDEXER_HEADS + threadIdx.x];
-  __syncthreads();
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
 
-  const int n_b = min((int64_t)__ldg(len + b), cap);  // never past the capacity
-  const int n = cand ? P : n_b;
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  int64_t pos = i;
-  if (cand) {
-    pos = __ldg(cand + (size_t)b * P + i);
-    if (pos < 0 || pos >= n_b) {
-      if (pos >= n_b) set_dev_error(CSA2_ERR_BOUNDS);
-      scores[(size_t)b * stride + i] = -INFINITY;
-      return;
+// 32-bit read-only load, L2 evict-first (the keys are streamed once).
+__device__ __forceinline__ uint32_t ldg_stream_u32(const void* p, uint64_t pol) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;\n" : "=r"(v) : "l"(p), "l"(pol));
+  return v;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
+// Four bytes = eight E2M1 codes -> four f16x2 (the low nibble of a byte in the low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n .reg .b8 c0, c1, c2, c3;\n"
+      " mov.b32 {c0, c1, c2, c3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, c0;\n"
+      " cvt.rn.f16x2.e2m1x2 %1, c1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, c2;\n"
+      " cvt.rn.f16x2.e2m1x2 %3, c3;\n}\n"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 2^(e-127) for an E8M0 byte (e < 255); byte 0 is the subnormal 2^-127.
+__device__ __forceinline__ float e8m0_value(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+// ------------------------------------------------------------------ tile registers
+struct ScanTile {
+  uint32_t w[4][4];  // [row r = entry g + 8r][block j]: code word t4 of block j
+  uint32_t s[4];     // the entry's four E8M0 bytes, shifted right by 8*(t4>>1)
+  int b;             // sequence
+  int64_t e0;        // first entry (or candidate slot) of the tile
+  uint32_t flags;    // bit r: slot in range; bit 4+r: entry valid
+};
+
+struct ScanArgs {
+  const void* q_idx;
+  int q_dtype;
+  const float* w;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  int64_t cap;
+  const int32_t* len;
+  const int32_t* cand;
+  int P;
+  float* scores;
+  int64_t stride;
+  int64_t tiles_per_seq;
+  int64_t total_tiles;
+};
+
+__device__ __forceinline__ void scan_load_tile(ScanTile& T, int64_t t, const ScanArgs& a, int g, int t4,
+                                               uint64_t pol) {
+  T.b = (int)(t / a.tiles_per_seq);
+  T.e0 = (t - (int64_t)T.b * a.tiles_per_seq) * kScanTile;
+  const int64_t n_b = min((int64_t)__ldg(a.len + T.b), a.cap);
+  const int64_t n = a.cand ? (int64_t)a.P : n_b;
+  T.flags = 0;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int64_t e = T.e0 + g + 8 * r;
+    int64_t pos = e;
+    bool in = e < n, ok = in;
+    if (a.cand && in) {
+      pos = __ldg(a.cand + (size_t)T.b * a.P + e);
+      ok = pos >= 0 && pos < n_b;
+      if (pos >= n_b && t4 == 0) set_dev_error(CSA2_ERR_BOUNDS);
+    }
+    T.flags |= (in ? 1u : 0u) << r;
+    T.flags |= (ok ? 1u : 0u) << (4 + r);
+    if (ok) {
+      const size_t row = (size_t)T.b * a.cap + pos;
+      const uint8_t* cp = a.codes + row * 64 + 4 * t4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) T.w[r][j] = ldg_stream_u32(cp + 16 * j, pol);
+      T.s[r] = ldg_stream_u32(a.scales + row * 4, pol) >> (8 * (t4 >> 1));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) T.w[r][j] = 0;
+      T.s[r] = 0;
     }
   }
-  const size_t row = (size_t)b * cap + pos;
-  const uint4* cp = reinterpret_cast<const uint4*>(codes + row * 64);
-  const uint32_t sc = __ldg(reinterpret_cast<const uint32_t*>(scales + row * 4));
-  float acc[CSA2_INDEXER_HEADS] = {0.f, 0.f, 0.f, 0.f};
+}
+
+// Query fragments of sequence b. NPART = 1 (bf16 queries) or 2 (fp32: hi, lo).
+template <int NPART>
+__device__ __forceinline__ void scan_setup(int b, const ScanArgs& a, int lane, int g, int t4,
+                                           uint32_t (&bf)[2][4][NPART][2], float& wsel0, float& wsel1) {
+  const size_t qb = (size_t)b * CSA2_INDEXER_HEADS * CSA2_INDEXER_DIM;
+  float f[CSA2_INDEXER_HEADS], winv[CSA2_INDEXER_HEADS];
 #pragma unroll
-  for (int blk = 0; blk < 4; ++blk) {
-    const uint4 v = __ldg(cp + blk);
-    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-    float part[CSA2_INDEXER_HEADS] = {0.f, 0.f, 0.f, 0.f};
+  for (int h = 0; h < CSA2_INDEXER_HEADS; ++h) {
+    float m = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {  // channel 32*blk + j, nibble j of the block's 16 bytes
-      const uint32_t c = (wd[j >> 3] >> (4 * (j & 7))) & 15u;
-      float val = e2m1_magnitude(c & 7u);
-      val = (c & 8u) ? -val : val;
-#pragma unroll
-      for (int h = 0; h < CSA2_INDEXER_HEADS; ++h) part[h] = fmaf(qs[h][32 * blk + j], val, part[h]);
+    for (int i = 0; i < 4; ++i) m = fmaxf(m, fabsf(load_elem(a.q_idx, a.q_dtype, qb + h * 128 + lane + 32 * i)));
+    m = warp_max(m);
+    int s = 0;
+    if (m > 0.f) {
+      const int e = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;  // floor(log2 m) for normal m
+      s = min(max(14 - e, -100), 100);
     }
-    const float s = e8m0_decode((sc >> (8 * blk)) & 0xFFu);
-#pragma unroll
-    for (int h = 0; h < CSA2_INDEXER_HEADS; ++h) acc[h] = fmaf(part[h], s, acc[h]);
+    f[h] = __uint_as_float((uint32_t)(127 + s) << 23);     // 2^s, exact
+    winv[h] = __ldg(a.w + (size_t)b * CSA2_INDEXER_HEADS + h) * __uint_as_float((uint32_t)(127 - s) << 23);
   }
-  float score = 0.f;
+  const int h0 = 2 * (t4 & 1);
+  wsel0 = (h0 == 0) ? winv[0] : winv[2];
+  wsel1 = (h0 == 0) ? winv[1] : winv[3];
+  // column n = g: jj = g >> 2 (block of the pair), head hh = g & 3
+  const int jj = g >> 2, hh = g & 3;
+  float fh = f[0];
 #pragma unroll
-  for (int h = 0; h < CSA2_INDEXER_HEADS; ++h) score = fmaf(ws[h], fmaxf(acc[h], 0.f), score);
-  scores[(size_t)b * stride + i] = score;
+  for (int h = 1; h < CSA2_INDEXER_HEADS; ++h) fh = hh == h ? f[h] : fh;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+#pragma unroll
+    for (int kq = 0; kq < 4; ++kq) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // b0: block 2p (jj == 0), b1: block 2p+1 (jj == 1)
+        const int c = 64 * p + 32 * half + 8 * t4 + 2 * kq;
+        const bool live = jj == half;
+        float x0 = 0.f, x1 = 0.f;
+        if (live) {
+          x0 = load_elem(a.q_idx, a.q_dtype, qb + hh * 128 + c) * fh;
+          x1 = load_elem(a.q_idx, a.q_dtype, qb + hh * 128 + c + 1) * fh;
+        }
+        const float h0v = __half2float(__float2half_rn(x0)), h1v = __half2float(__float2half_rn(x1));
+        bf[p][kq][0][half] = f16x2_bits(h0v, h1v);
+        if constexpr (NPART == 2) bf[p][kq][NPART - 1][half] = f16x2_bits(x0 - h0v, x1 - h1v);
+      }
+    }
+  }
+}
+
+template <int NPART>
+__global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan(const ScanArgs a) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int64_t gw = (int64_t)blockIdx.x * kScanWarps + (threadIdx.x >> 5);
+  const int64_t nw = (int64_t)gridDim.x * kScanWarps;
+  const int64_t t_begin = gw * a.total_tiles / nw, t_end = (gw + 1) * a.total_tiles / nw;
+  if (t_begin >= t_end) return;
+  const uint64_t pol = l2_evict_first_policy();
+
+  uint32_t bf[2][4][NPART][2];
+  float wsel0 = 0.f, wsel1 = 0.f;
+  int setup_b = -1;
+
+  ScanTile cur, nxt;
+  scan_load_tile(cur, t_begin, a, g, t4, pol);
+  for (int64_t t = t_begin; t < t_end; ++t) {
+    if (t + 1 < t_end) scan_load_tile(nxt, t + 1, a, g, t4, pol);
+    if (!a.cand && t + 2 < t_end) {  // warm L2 two tiles ahead (one 64-byte row per lane)
+      const int64_t t2 = t + 2;
+      const int b2 = (int)(t2 / a.tiles_per_seq);
+      const int64_t e2 = (t2 - (int64_t)b2 * a.tiles_per_seq) * kScanTile + lane;
+      if (e2 < a.cap) prefetch_l2(a.codes + ((size_t)b2 * a.cap + e2) * 64);
+    }
+    if (cur.b != setup_b) {
+      scan_setup<NPART>(cur.b, a, lane, g, t4, bf, wsel0, wsel1);
+      setup_b = cur.b;
+    }
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {  // two m16 row tiles: rows (2st, 2st+1) = entries g + 16st (+8)
+      const int rl = 2 * st, rh = 2 * st + 1;
+      float acc[2][NPART][4];
+#pragma unroll
+      for (int p = 0; p < 2; ++p)
+#pragma unroll
+        for (int nt = 0; nt < NPART; ++nt) acc[p][nt][0] = acc[p][nt][1] = acc[p][nt][2] = acc[p][nt][3] = 0.f;
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        uint32_t lo0[4], lo1[4], hi0[4], hi1[4];
+        e2m1x8_to_f16x2(cur.w[rl][2 * p], lo0);
+        e2m1x8_to_f16x2(cur.w[rl][2 * p + 1], lo1);
+        e2m1x8_to_f16x2(cur.w[rh][2 * p], hi0);
+        e2m1x8_to_f16x2(cur.w[rh][2 * p + 1], hi1);
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq)
+#pragma unroll
+          for (int nt = 0; nt < NPART; ++nt)
+            mma_16816(acc[p][nt], lo0[kq], hi0[kq], lo1[kq], hi1[kq], bf[p][kq][nt][0], bf[p][kq][nt][1]);
+      }
+      // epilogue: this lane's columns 2t4, 2t4+1 = block 2p + (t4>>1), heads 2(t4&1) + {0,1}
+      float v[2][2];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const uint32_t sw = cur.s[rr ? rh : rl];
+        const float sc0 = e8m0_value(sw & 0xFFu), sc1 = e8m0_value((sw >> 16) & 0xFFu);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float c0 = acc[0][0][2 * rr + e], c1 = acc[1][0][2 * rr + e];
+          if constexpr (NPART == 2) {
+            c0 += acc[0][1][2 * rr + e];
+            c1 += acc[1][1][2 * rr + e];
+          }
+          v[rr][e] = fmaf(c1, sc1, c0 * sc0);
+        }
+      }
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) v[rr][e] += __shfl_xor_sync(0xffffffffu, v[rr][e], 2);
+      float part[2];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        part[rr] = fmaf(wsel1, fmaxf(v[rr][1], 0.f), wsel0 * fmaxf(v[rr][0], 0.f));
+        part[rr] += __shfl_xor_sync(0xffffffffu, part[rr], 1);
+      }
+      // lane t4 == 0 stores row g + 16st, lane t4 == 1 row g + 16st + 8
+      if (t4 < 2) {
+        const int r = t4 ? rh : rl;
+        if ((cur.flags >> r) & 1u) {
+          const int64_t e = cur.e0 + g + 8 * r;
+          a.scores[(size_t)cur.b * a.stride + e] = ((cur.flags >> (4 + r)) & 1u) ? (t4 ? part[1] : part[0]) : -INFINITY;
+        }
+      }
+    }
+    cur = nxt;
+  }
 }
 
 }  // namespace csa2

@@ -204,3 +204,34 @@ def test_attention_index_past_len_is_flagged():
     K.sparse_latent_attn(q, cache, idx)
     assert K.sync_status() == K.A.ERR_BOUNDS
     assert K.sync_status() == 0
+
+
+@pytest.mark.parametrize("sampled_high", [True, False])
+def test_topk_unrepresentative_sample_takes_the_exact_fallback(sampled_high):
+    """Scores built so that the evenly spaced sample misleads the threshold: either
+    too few (sampled slots high) or too many (sampled slots low) keys pass the
+    filter. The result must still be the exact Top-k."""
+    B, n, k = 2, 131072, 512
+    S = 4096  # sample size used for k <= 1024
+    s = WL.scores(11, B, n, device="cpu") * 0.5 + 0.25
+    sampled = (torch.arange(S) * n) // S
+    if sampled_high:
+        s[:, sampled] += 1.0          # only ~r slots reach the sampled threshold
+    else:
+        s[:, sampled] -= 0.25         # nearly every slot beats the sampled threshold
+    out = K.topk_select(s.cuda(), k)
+    torch.cuda.synchronize()
+    for b in range(B):
+        ref = O.topk_positions(s[b].numpy().astype(np.float64), k)
+        assert np.array_equal(np_(out[b]), ref)
+
+
+@pytest.mark.parametrize("n,k", [(524288, 16384), (65536 + 77, 512), (20000, 1500)])
+def test_topk_large_rows(n, k):
+    B = 2
+    s = WL.scores(n + k, B, n, device="cpu", ties=100000)
+    out = K.topk_select(s.cuda(), k)
+    torch.cuda.synchronize()
+    for b in range(B):
+        ref = O.topk_positions(s[b].numpy().astype(np.float64), k)
+        assert np.array_equal(np_(out[b]), ref)
