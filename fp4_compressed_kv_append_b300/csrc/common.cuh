@@ -115,6 +115,9 @@ __device__ __forceinline__ uint32_t float_order_key(float s) {
 }
 
 // ---------------------------------------------------------------- misc
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint32_t smem_u32addr(const void* p) { return smem_u32(p); }
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

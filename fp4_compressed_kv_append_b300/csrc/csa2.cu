@@ -4,6 +4,8 @@
 #include <atomic>
 #include <cstring>
 
+#include <cuda.h>
+
 #include "common.cuh"
 #include "quant_append.cuh"
 #include "indexer_scan.cuh"
@@ -73,22 +75,84 @@ int sm_count() {
 }
 
 template <int NPART>
-void launch_scan_t(const ScanArgs& a, cudaStream_t s) {
+void launch_scan_gather(const ScanArgs& a, cudaStream_t s) {
   static int per_sm = 0;
   if (per_sm == 0) {
     int occ = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_indexer_scan<NPART>, kScanThreads, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_indexer_scan_gather<NPART>, kScanThreads, 0);
     per_sm = occ > 0 ? occ : 1;
   }
   const int64_t want = (a.total_tiles + kScanWarps - 1) / kScanWarps;  // >= 1 tile per warp
   const int64_t full = (int64_t)sm_count() * per_sm;
   const int grid = (int)(want < full ? want : full);
-  k_indexer_scan<NPART><<<grid, kScanThreads, 0, s>>>(a);
+  k_indexer_scan_gather<NPART><<<grid, kScanThreads, 0, s>>>(a);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Tensor map of the key codes viewed as rows x 64 bytes; box 128 rows, 64-byte swizzle.
+bool make_codes_map(CUtensorMap* m, const uint8_t* codes, int64_t rows) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc || rows <= 0 || rows >= ((int64_t)1 << 31)) return false;
+  const cuuint64_t gdim[2] = {64, (cuuint64_t)rows};
+  const cuuint64_t gstride[1] = {64};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kTmaRows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), gdim, gstride, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NPART>
+void launch_scan_tma(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(k_indexer_scan_tma<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem);
+    attr_set = true;
+  }
+  const int64_t full = (int64_t)sm_count() * 2;
+  const int grid = (int)(a.total_tiles < full ? a.total_tiles : full);
+  k_indexer_scan_tma<NPART><<<grid, kTmaThreads, kTmaSmem, s>>>(m, a);
 }
 
 void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
                  int64_t cap, const int32_t* len, const int32_t* cand, int P, float* scores, int batch,
                  cudaStream_t s) {
+  g_launches += 1;
+  CUtensorMap m;
+  if (!cand && cap % kTmaRows == 0 && make_codes_map(&m, codes, (int64_t)batch * cap)) {
+    TmaScanArgs t;
+    t.q_idx = q_idx;
+    t.q_dtype = (int)dt;
+    t.w = w;
+    t.codes = codes;
+    t.scales = scales;
+    t.cap = cap;
+    t.len = len;
+    t.scores = scores;
+    t.tiles_per_seq = cap / kTmaRows;
+    t.total_tiles = t.tiles_per_seq * batch;
+    if (dt == CSA2_F32) launch_scan_tma<2>(m, t, s);
+    else launch_scan_tma<1>(m, t, s);
+    return;
+  }
   ScanArgs a;
   a.q_idx = q_idx;
   a.q_dtype = (int)dt;
@@ -103,9 +167,8 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
   a.stride = cand ? P : cap;
   a.tiles_per_seq = (a.stride + kScanTile - 1) / kScanTile;
   a.total_tiles = a.tiles_per_seq * batch;
-  if (dt == CSA2_F32) launch_scan_t<2>(a, s);
-  else launch_scan_t<1>(a, s);
-  g_launches += 1;
+  if (dt == CSA2_F32) launch_scan_gather<2>(a, s);
+  else launch_scan_gather<1>(a, s);
 }
 
 void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,

@@ -27,6 +27,8 @@
 // tiles), prefetching the next tile's registers while it computes the current one.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace csa2 {
@@ -79,9 +81,11 @@ __device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// 2^(e-127) for an E8M0 byte (e < 255); byte 0 is the subnormal 2^-127.
-__device__ __forceinline__ float e8m0_value(uint32_t e) {
-  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+// 2^(e-127) for the E8M0 byte e = bits [7:0] of w (e < 255): the byte moved to the
+// float exponent field; byte 0 becomes the subnormal 2^-127 (bit pattern 0x00400000,
+// the unsigned maximum of the two, since every e >= 1 gives at least 0x00800000).
+__device__ __forceinline__ float e8m0_low_byte(uint32_t w) {
+  return __uint_as_float(max((w << 23) & 0x7F800000u, 0x00400000u));
 }
 
 // ------------------------------------------------------------------ tile registers
@@ -191,8 +195,67 @@ __device__ __forceinline__ void scan_setup(int b, const ScanArgs& a, int lane, i
   }
 }
 
+// One m16 row tile: rows g (words wl, scale word sl) and g+8 (wh, sh) of a
+// 16-entry group. Returns the scores of both rows (in every lane of the quad).
 template <int NPART>
-__global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan(const ScanArgs a) {
+__device__ __forceinline__ void scan_m16(const uint32_t (&wl)[4], const uint32_t (&wh)[4], uint32_t sl, uint32_t sh,
+                                         const uint32_t (&bf)[2][4][NPART][2], float wsel0, float wsel1,
+                                         float& score_lo, float& score_hi) {
+  float acc[2][NPART][4];
+#pragma unroll
+  for (int p = 0; p < 2; ++p)
+#pragma unroll
+    for (int nt = 0; nt < NPART; ++nt) acc[p][nt][0] = acc[p][nt][1] = acc[p][nt][2] = acc[p][nt][3] = 0.f;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    uint32_t lo0[4], lo1[4], hi0[4], hi1[4];
+    e2m1x8_to_f16x2(wl[2 * p], lo0);
+    e2m1x8_to_f16x2(wl[2 * p + 1], lo1);
+    e2m1x8_to_f16x2(wh[2 * p], hi0);
+    e2m1x8_to_f16x2(wh[2 * p + 1], hi1);
+#pragma unroll
+    for (int kq = 0; kq < 4; ++kq)
+#pragma unroll
+      for (int nt = 0; nt < NPART; ++nt)
+        mma_16816(acc[p][nt], lo0[kq], hi0[kq], lo1[kq], hi1[kq], bf[p][kq][nt][0], bf[p][kq][nt][1]);
+  }
+  // this lane's columns 2t4, 2t4+1 = block 2p + (t4>>1), heads 2(t4&1) + {0,1};
+  // sl/sh hold the entry's scale bytes shifted right by 8*(t4>>1)
+  float v[2][2];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const uint32_t sw = rr ? sh : sl;
+    const float sc0 = e8m0_low_byte(sw), sc1 = e8m0_low_byte(sw >> 16);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float c0 = acc[0][0][2 * rr + e], c1 = acc[1][0][2 * rr + e];
+      if constexpr (NPART == 2) {
+        c0 += acc[0][1][2 * rr + e];
+        c1 += acc[1][1][2 * rr + e];
+      }
+      v[rr][e] = fmaf(c1, sc1, c0 * sc0);
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) v[rr][e] += __shfl_xor_sync(0xffffffffu, v[rr][e], 2);
+  float part[2];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    part[rr] = fmaf(wsel1, fmaxf(v[rr][1], 0.f), wsel0 * fmaxf(v[rr][0], 0.f));
+    part[rr] += __shfl_xor_sync(0xffffffffu, part[rr], 1);
+  }
+  score_lo = part[0];
+  score_hi = part[1];
+}
+
+// ---------------------------------------------------------------- gather form
+// Scores a list of candidate positions (the hierarchical pool): rows are
+// gathered, so each lane loads its words straight from global memory, one
+// 32-entry tile ahead.
+template <int NPART>
+__global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan_gather(const ScanArgs a) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int64_t gw = (int64_t)blockIdx.x * kScanWarps + (threadIdx.x >> 5);
   const int64_t nw = (int64_t)gridDim.x * kScanWarps;
@@ -208,73 +271,237 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan(const ScanArgs
   scan_load_tile(cur, t_begin, a, g, t4, pol);
   for (int64_t t = t_begin; t < t_end; ++t) {
     if (t + 1 < t_end) scan_load_tile(nxt, t + 1, a, g, t4, pol);
-    if (!a.cand && t + 2 < t_end) {  // warm L2 two tiles ahead (one 64-byte row per lane)
-      const int64_t t2 = t + 2;
-      const int b2 = (int)(t2 / a.tiles_per_seq);
-      const int64_t e2 = (t2 - (int64_t)b2 * a.tiles_per_seq) * kScanTile + lane;
-      if (e2 < a.cap) prefetch_l2(a.codes + ((size_t)b2 * a.cap + e2) * 64);
-    }
     if (cur.b != setup_b) {
       scan_setup<NPART>(cur.b, a, lane, g, t4, bf, wsel0, wsel1);
       setup_b = cur.b;
     }
 #pragma unroll
-    for (int st = 0; st < 2; ++st) {  // two m16 row tiles: rows (2st, 2st+1) = entries g + 16st (+8)
+    for (int st = 0; st < 2; ++st) {  // rows (2st, 2st+1) = entries g + 16st (+8)
       const int rl = 2 * st, rh = 2 * st + 1;
-      float acc[2][NPART][4];
-#pragma unroll
-      for (int p = 0; p < 2; ++p)
-#pragma unroll
-        for (int nt = 0; nt < NPART; ++nt) acc[p][nt][0] = acc[p][nt][1] = acc[p][nt][2] = acc[p][nt][3] = 0.f;
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        uint32_t lo0[4], lo1[4], hi0[4], hi1[4];
-        e2m1x8_to_f16x2(cur.w[rl][2 * p], lo0);
-        e2m1x8_to_f16x2(cur.w[rl][2 * p + 1], lo1);
-        e2m1x8_to_f16x2(cur.w[rh][2 * p], hi0);
-        e2m1x8_to_f16x2(cur.w[rh][2 * p + 1], hi1);
-#pragma unroll
-        for (int kq = 0; kq < 4; ++kq)
-#pragma unroll
-          for (int nt = 0; nt < NPART; ++nt)
-            mma_16816(acc[p][nt], lo0[kq], hi0[kq], lo1[kq], hi1[kq], bf[p][kq][nt][0], bf[p][kq][nt][1]);
-      }
-      // epilogue: this lane's columns 2t4, 2t4+1 = block 2p + (t4>>1), heads 2(t4&1) + {0,1}
-      float v[2][2];
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const uint32_t sw = cur.s[rr ? rh : rl];
-        const float sc0 = e8m0_value(sw & 0xFFu), sc1 = e8m0_value((sw >> 16) & 0xFFu);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float c0 = acc[0][0][2 * rr + e], c1 = acc[1][0][2 * rr + e];
-          if constexpr (NPART == 2) {
-            c0 += acc[0][1][2 * rr + e];
-            c1 += acc[1][1][2 * rr + e];
-          }
-          v[rr][e] = fmaf(c1, sc1, c0 * sc0);
-        }
-      }
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) v[rr][e] += __shfl_xor_sync(0xffffffffu, v[rr][e], 2);
-      float part[2];
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        part[rr] = fmaf(wsel1, fmaxf(v[rr][1], 0.f), wsel0 * fmaxf(v[rr][0], 0.f));
-        part[rr] += __shfl_xor_sync(0xffffffffu, part[rr], 1);
-      }
-      // lane t4 == 0 stores row g + 16st, lane t4 == 1 row g + 16st + 8
-      if (t4 < 2) {
+      float s_lo, s_hi;
+      scan_m16<NPART>(cur.w[rl], cur.w[rh], cur.s[rl], cur.s[rh], bf, wsel0, wsel1, s_lo, s_hi);
+      if (t4 < 2) {  // lane t4 == 0 stores row rl, lane t4 == 1 row rh
         const int r = t4 ? rh : rl;
         if ((cur.flags >> r) & 1u) {
           const int64_t e = cur.e0 + g + 8 * r;
-          a.scores[(size_t)cur.b * a.stride + e] = ((cur.flags >> (4 + r)) & 1u) ? (t4 ? part[1] : part[0]) : -INFINITY;
+          a.scores[(size_t)cur.b * a.stride + e] = ((cur.flags >> (4 + r)) & 1u) ? (t4 ? s_hi : s_lo) : -INFINITY;
         }
       }
     }
     cur = nxt;
+  }
+}
+
+// ---------------------------------------------------------------- streaming form
+// Scores every entry of every sequence. A producer warp streams 128-entry tiles
+// of codes (one TMA box of 128 rows x 64 bytes, 64-byte swizzle) and their E8M0
+// bytes (one 512-byte bulk copy) into a ring of shared-memory stages; eight
+// consumer warps take 16 rows each per stage. Full/empty mbarriers hand the
+// stages back and forth; every wait gives up after about a second, records
+// CSA2_ERR_TIMEOUT and stops the block.
+//
+// With the 64-byte swizzle the 16-byte chunk j of row r sits at chunk
+// j ^ ((r >> 1) & 3), which makes the consumers' 32-bit loads (word t4 of each
+// chunk, rows g and g+8) free of bank conflicts.
+constexpr int kTmaConsumers = 8;
+constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
+constexpr int kTmaRows = 128;
+constexpr int kTmaStages = 8;
+constexpr int kTmaStageBytes = 9216;  // 8192 code bytes (1024-aligned) + 512 scale bytes
+constexpr int kTmaSmem = kTmaStages * kTmaStageBytes + 2 * kTmaStages * 8 + 64 + 1024;
+
+struct TmaScanArgs {
+  const void* q_idx;
+  int q_dtype;
+  const float* w;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  int64_t cap;
+  const int32_t* len;
+  float* scores;
+  int64_t tiles_per_seq;  // cap / 128
+  int64_t total_tiles;
+};
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of the given parity; false after ~1 s (error recorded) or
+// when another thread of the block has given up (*abort set).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > 1000000000ull) {
+        set_dev_error(CSA2_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+template <int NPART>
+__global__ void __launch_bounds__(kTmaThreads, 2)
+k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32addr(smem);
+  const uint32_t bar_full = sbase + kTmaStages * kTmaStageBytes;
+  const uint32_t bar_empty = bar_full + 8 * kTmaStages;
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + kTmaStages * kTmaStageBytes + 16 * kTmaStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTmaStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kTmaConsumers);
+    }
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+
+  const int64_t t_begin = (int64_t)blockIdx.x * a.total_tiles / gridDim.x;
+  const int64_t t_end = (int64_t)(blockIdx.x + 1) * a.total_tiles / gridDim.x;
+  int b0 = (int)(t_begin / a.tiles_per_seq);
+  int64_t e00 = (t_begin - (int64_t)b0 * a.tiles_per_seq) * kTmaRows;
+
+  if (warp == kTmaConsumers) {
+    // ---------------- producer (one lane)
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      asm volatile("prefetch.tensormap [%0];\n" ::"l"(&tmap) : "memory");
+      uint32_t it = 0;
+      int b = b0;
+      int64_t e0 = e00;
+      int64_t n_b = min((int64_t)__ldg(a.len + b), a.cap);
+      for (int64_t t = t_begin; t < t_end; ++t) {
+        if (e0 < n_b) {
+          const uint32_t s = it % kTmaStages, ph = (it / kTmaStages) & 1u;
+          if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort)) break;
+          const uint32_t st = sbase + s * kTmaStageBytes;
+          const int64_t row = (int64_t)b * a.cap + e0;
+          mbar_arrive_expect_tx(bar_full + 8 * s, kTmaRows * 64 + kTmaRows * 4);
+          tma_load_rows(st, &tmap, 0, (int32_t)row, bar_full + 8 * s, pol);
+          bulk_load(st + kTmaRows * 64, a.scales + row * 4, kTmaRows * 4, bar_full + 8 * s, pol);
+          ++it;
+        }
+        e0 += kTmaRows;
+        if (e0 >= a.tiles_per_seq * kTmaRows && t + 1 < t_end) {
+          e0 = 0;
+          ++b;
+          n_b = min((int64_t)__ldg(a.len + b), a.cap);
+        }
+      }
+      // drain: every issued stage must land before the block exits
+      for (uint32_t j = (it > kTmaStages ? it - kTmaStages : 0); j < it; ++j) {
+        volatile int no_abort = 0;
+        mbar_wait_bounded(bar_full + 8 * (j % kTmaStages), (j / kTmaStages) & 1u, &no_abort);
+      }
+    }
+  } else {
+    // ---------------- consumers: warp w owns rows 16w .. 16w+15 of every stage
+    const int g = lane >> 2, t4 = lane & 3;
+    const int rl = 16 * warp + g, rh = rl + 8;
+    const uint32_t swz = (uint32_t)((g >> 1) & 3);  // same for rl and rh
+    ScanArgs sa;
+    sa.q_idx = a.q_idx;
+    sa.q_dtype = a.q_dtype;
+    sa.w = a.w;
+    uint32_t bf[2][4][NPART][2];
+    float wsel0 = 0.f, wsel1 = 0.f;
+    int setup_b = -1;
+    uint32_t it = 0;
+    int b = b0;
+    int64_t e0 = e00;
+    int64_t n_b = min((int64_t)__ldg(a.len + b), a.cap);
+    for (int64_t t = t_begin; t < t_end; ++t) {
+      if (e0 < n_b) {
+        if (b != setup_b) {
+          scan_setup<NPART>(b, sa, lane, g, t4, bf, wsel0, wsel1);
+          setup_b = b;
+        }
+        const uint32_t s = it % kTmaStages, ph = (it / kTmaStages) & 1u;
+        if (!mbar_wait_bounded(bar_full + 8 * s, ph, abort)) break;
+        const unsigned char* st = smem + s * kTmaStageBytes;
+        uint32_t wl[4], wh[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t off = 16u * ((uint32_t)j ^ swz) + 4u * t4;
+          wl[j] = *reinterpret_cast<const uint32_t*>(st + 64 * rl + off);
+          wh[j] = *reinterpret_cast<const uint32_t*>(st + 64 * rh + off);
+        }
+        const uint32_t sl = *reinterpret_cast<const uint32_t*>(st + kTmaRows * 64 + 4 * rl) >> (8 * (t4 >> 1));
+        const uint32_t sh = *reinterpret_cast<const uint32_t*>(st + kTmaRows * 64 + 4 * rh) >> (8 * (t4 >> 1));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        ++it;
+        float s_lo, s_hi;
+        scan_m16<NPART>(wl, wh, sl, sh, bf, wsel0, wsel1, s_lo, s_hi);
+        if (t4 < 2) {
+          const int64_t e = e0 + (t4 ? rh : rl);
+          if (e < n_b) a.scores[(size_t)b * a.cap + e] = t4 ? s_hi : s_lo;
+        }
+      }
+      e0 += kTmaRows;
+      if (e0 >= a.tiles_per_seq * kTmaRows && t + 1 < t_end) {
+        e0 = 0;
+        ++b;
+        n_b = min((int64_t)__ldg(a.len + b), a.cap);
+      }
+    }
   }
 }
 

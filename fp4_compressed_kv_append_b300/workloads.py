@@ -125,3 +125,20 @@ def scores(seed: int, B: int, n: int, device="cpu", ties: int = 0):
     if ties:
         s = torch.floor(s * ties) / ties
     return s
+
+
+def random_cache_bytes(seed: int, B: int, cap: int, device="cpu", scale_lo: int = 120, scale_hi: int = 135):
+    """Uniformly random packed cache bytes for kernel timing (every byte pattern is a
+    valid pair of E2M1 codes). Scales: E8M0 bytes in [scale_lo, scale_hi) for the keys,
+    E4M3 bytes 0x30..0x4F (about 0.5 to 16) for the latent.
+
+    Returns (lat_codes [B,cap,256], lat_scales [B,cap,32], idx_codes [B,cap,64],
+    idx_scales [B,cap,4]) uint8.
+    """
+    g = generator(seed, "random-cache", device=device)
+    u8 = dict(dtype=torch.uint8, device=device, generator=g)
+    lat_codes = torch.randint(0, 256, (B, cap, 256), **u8)
+    lat_scales = torch.randint(0x30, 0x50, (B, cap, 32), **u8)
+    idx_codes = torch.randint(0, 256, (B, cap, 64), **u8)
+    idx_scales = torch.randint(scale_lo, scale_hi, (B, cap, 4), **u8)
+    return lat_codes, lat_scales, idx_codes, idx_scales
