@@ -6,14 +6,22 @@
 // token", "Troisiemement" (E2M1 values with an E4M3 scale per 16 channels; a
 // 128-token sliding window kept outside the global cache).
 //
-// Split-key ("flash-decoding") form: one 256-thread block per (sequence, 128 keys).
-// The block dequantises its 128 keys to fp16 in shared memory -- exact, since an
-// E2M1 value times an E4M3 scale has at most 6 significant bits and lies in
-// [2^-10, 2688] -- and runs S = Q V^T and O = P V on the tensor cores
-// (mma.sync m16n8k16, fp16 inputs, fp32 accumulation). Queries are scaled per head
-// by a power of two so that fp16 keeps their bits; that factor is undone on the
-// logits. fp32 queries are split into two fp16 parts (hi + lo). Each block writes an
-// unnormalised partial (o, running max m, sum l); k_attn_combine merges the splits.
+// One 256-thread block per (sequence, group of 16 heads) walks all selected keys,
+// then the window rows, in chunks of 64 with an online softmax -- no partial
+// results leave the block. Per chunk:
+//  * the raw codes and scales of the chunk's entries were gathered into shared
+//    memory by cp.async during the previous chunk; they are dequantised to fp16
+//    (exact: an E2M1 value times an E4M3 scale has at most 6 significant bits and
+//    lies in [2^-10, 2688]); window rows (bf16) are converted directly;
+//  * S = Q V^T on the tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate):
+//    warp (kg, dg) covers keys 32kg..32kg+31 over dims 128dg..128dg+127 with its
+//    query fragments held in registers; the four dim-group partials meet in
+//    shared memory;
+//  * softmax in base 2 with a running max per head; P is rounded to fp16;
+//  * O += P V, warp w owning output dims 64w..64w+63.
+// Queries are scaled per head by a power of two 2^s so that fp16 keeps their
+// bits (fp32 queries are split into fp16 hi + lo parts); the factor is undone in
+// the logit coefficient.
 #pragma once
 
 #include "common.cuh"
@@ -21,23 +29,22 @@
 namespace csa2 {
 
 constexpr int kAttnThreads = 256;  // 8 warps
-constexpr int kAttnKeys = 128;     // keys per block
+constexpr int kAttnChunk = 64;     // keys per chunk
+constexpr int kAttnHeads = 16;     // heads per block
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int HT>
-struct AttnShape {
-  static constexpr int H = 16 * HT;
-  static constexpr int NKG = 8 / HT;        // key groups (GEMM1) / dim groups (GEMM2)
-  static constexpr int KW = kAttnKeys / NKG;
-  static constexpr int NT1 = KW / 8;        // n8 tiles of S per warp
-  static constexpr int DW = 512 / NKG;
-  static constexpr int NT2 = DW / 8;        // n8 tiles of O per warp
-  static constexpr size_t q_bytes = (size_t)H * 1024;
-  static constexpr size_t v_bytes = (size_t)kAttnKeys * 1024;
-  static constexpr size_t p_bytes = (size_t)H * 256;
-  static constexpr size_t red_bytes = (size_t)2 * NKG * H * 4;
-  static constexpr size_t smem = q_bytes + v_bytes + p_bytes + red_bytes + H * 4 + kAttnKeys * 4;
-};
+// shared-memory layout (bytes)
+constexpr int kAttnV = 0;                                     // [64 keys][512] fp16, swizzled; Q first
+constexpr int kAttnRawC = kAttnV + kAttnChunk * 1024;         // [64][256] codes
+constexpr int kAttnRawS = kAttnRawC + kAttnChunk * 256;       // [64][32] E4M3 scales
+constexpr int kAttnSPitch = 68;                               // floats per S-partial row
+constexpr int kAttnSPart = kAttnRawS + kAttnChunk * 32;       // [4 dg][16 heads][68] f32
+constexpr int kAttnP = kAttnSPart + 4 * kAttnHeads * kAttnSPitch * 4;  // [16][64] fp16, swizzled
+constexpr int kAttnRedM = kAttnP + kAttnHeads * 128;          // [8 warps][16] f32
+constexpr int kAttnRedL = kAttnRedM + 8 * kAttnHeads * 4;     // [8 warps][16] f32
+constexpr int kAttnCoef = kAttnRedL + 8 * kAttnHeads * 4;     // [16] f32
+constexpr int kAttnKeyOk = kAttnCoef + kAttnHeads * 4;        // [64] i32
+constexpr int kAttnSmem = kAttnKeyOk + kAttnChunk * 4;
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk, int chunks_per_row) {
   return (uint32_t)(row * chunks_per_row * 16 + ((chunk ^ (row & 7)) << 4));
@@ -70,277 +77,339 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Write Q (one part) of sequence b into shared memory, scaled by 2^sq[h].
-// part 0: fp16(q*2^sq) (the only part for bf16 q); part 1: fp16 of the remainder.
-template <int H>
-__device__ void attn_load_q(const void* q, int q_dtype, int b, const float* sq_pow,
-                            unsigned char* qs, int part) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int h = wid; h < H; h += 8) {
-    const float f = sq_pow[h];
-    const size_t base = ((size_t)b * H + h) * 512 + 16 * lane;
-    uint32_t w[8];
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// Issue the gathers of the raw codes and scales of index chunk c.
+__device__ __forceinline__ void attn_prefetch_chunk(unsigned char* smem, const uint8_t* lat_codes,
+                                                    const uint8_t* lat_scales, const int32_t* idxrow, int k,
+                                                    int c, int n_b, size_t seq_row0) {
+  const int tid = threadIdx.x;
+  {
+    const int kk = tid >> 2, part = tid & 3;  // 4 x 64 bytes of codes per key
+    const int j = c * kAttnChunk + kk;
+    const int pos = j < k ? __ldg(idxrow + j) : -1;
+    if (pos >= 0 && pos < n_b) {
+      const uint8_t* src = lat_codes + (seq_row0 + pos) * 256 + 64 * part;
+      const uint32_t dst = smem_u32(smem + kAttnRawC + kk * 256 + 64 * part);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float v[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float x = load_elem(q, q_dtype, base + 2 * i + j) * f;
-        const float hi = __half2float(__float2half_rn(x));
-        v[j] = part == 0 ? hi : x - hi;
-      }
-      w[i] = pack_half2(v[0], v[1]);
+      for (int i = 0; i < 4; ++i) cp_async16(dst + 16 * i, src + 16 * i);
     }
-    // lane covers dims [16 lane, 16 lane + 16) = chunks 2 lane, 2 lane + 1
-    *reinterpret_cast<uint4*>(qs + swz(h, 2 * lane, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(qs + swz(h, 2 * lane + 1, 64)) = make_uint4(w[4], w[5], w[6], w[7]);
   }
+  if (tid < 2 * kAttnChunk) {
+    const int kk = tid >> 1, half = tid & 1;
+    const int j = c * kAttnChunk + kk;
+    const int pos = j < k ? __ldg(idxrow + j) : -1;
+    if (pos >= 0 && pos < n_b)
+      cp_async16(smem_u32(smem + kAttnRawS + kk * 32 + 16 * half), lat_scales + (seq_row0 + pos) * 32 + 16 * half);
+  }
+  cp_async_commit();
 }
 
-template <int HT>
-__global__ void __launch_bounds__(kAttnThreads, 1)
-k_sparse_attn_mma(const void* __restrict__ q, int q_dtype, float scale,
-                  const uint8_t* __restrict__ lat_codes, const uint8_t* __restrict__ lat_scales,
-                  const int32_t* __restrict__ len, int64_t cap, const int32_t* __restrict__ idx,
-                  int k, const uint16_t* __restrict__ swa, int W, int n_idx_splits,
-                  float* __restrict__ part_o, float* __restrict__ part_ml) {
-  using S = AttnShape<HT>;
-  constexpr int H = S::H;
+template <int NPART>
+__global__ void __launch_bounds__(kAttnThreads, NPART == 1 ? 2 : 1)
+k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_t* __restrict__ lat_codes,
+              const uint8_t* __restrict__ lat_scales, const int32_t* __restrict__ len, int64_t cap,
+              const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int W, int H,
+              float* __restrict__ out) {
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* qs = smem;
-  unsigned char* vs = qs + S::q_bytes;
-  unsigned char* ps = vs + S::v_bytes;
-  float* red_m = reinterpret_cast<float*>(ps + S::p_bytes);
-  float* red_l = red_m + S::NKG * H;
-  float* sq_pow = red_l + S::NKG * H;                 // per-head 2^sq
-  int* key_ok = reinterpret_cast<int*>(sq_pow + H);   // per key: 1 valid, 0 empty
+  unsigned char* vs = smem + kAttnV;
+  float* spart = reinterpret_cast<float*>(smem + kAttnSPart);
+  unsigned char* ps = smem + kAttnP;
+  float* red_m = reinterpret_cast<float*>(smem + kAttnRedM);
+  float* red_l = reinterpret_cast<float*>(smem + kAttnRedL);
+  float* coef = reinterpret_cast<float*>(smem + kAttnCoef);
+  int* key_ok = reinterpret_cast<int*>(smem + kAttnKeyOk);
 
-  const int b = blockIdx.y, split = blockIdx.x, n_splits = gridDim.x;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int hg = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
+  const int kg = w & 1, dg = w >> 1;
+  const int n_b = (int)min((int64_t)__ldg(len + b), cap);
+  const size_t seq_row0 = (size_t)b * cap;
+  const int32_t* idxrow = idx ? idx + (size_t)b * k : nullptr;
+  const int n_idx_chunks = (k + kAttnChunk - 1) / kAttnChunk;
+  const int n_chunks = n_idx_chunks + (W + kAttnChunk - 1) / kAttnChunk;
 
-  // ---- per-head power-of-two scale of the queries
-  for (int h = wid; h < H; h += 8) {
-    float mx = 0.f;
-    const size_t base = ((size_t)b * H + h) * 512;
-    for (int d = lane; d < 512; d += 32) mx = fmaxf(mx, fabsf(load_elem(q, q_dtype, base + d)));
-    mx = warp_max(mx);
-    if (lane == 0) {
-      int sq = 0;
-      if (mx > 0.f) {
-        const int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2) for normals
-        sq = min(max(14 - e, -100), 100);
-      }
-      sq_pow[h] = __uint_as_float((uint32_t)(sq + 127) << 23);  // exact 2^sq
-    }
-  }
+  if (n_idx_chunks > 0) attn_prefetch_chunk(smem, lat_codes, lat_scales, idxrow, k, 0, n_b, seq_row0);
 
-  // ---- the 128 keys of this split, dequantised to fp16 (rows swizzled)
-  const bool window_split = split >= n_idx_splits;
-  const int n_b = (int)min((int64_t)__ldg(len + b), cap);  // never past the capacity
+  // ---- queries: per-head 2^s, fp16 parts into the V area, then register fragments
   {
-    const int kk = tid >> 1, hf = tid & 1;
-    bool ok = false;
-    if (!window_split) {
-      const int j = split * kAttnKeys + kk;
-      const int pos = j < k ? __ldg(idx + (size_t)b * k + j) : -1;
-      if (pos >= n_b) set_dev_error(CSA2_ERR_BOUNDS);
-      ok = pos >= 0 && pos < n_b;
-      if (ok) {
-        const size_t row = (size_t)b * cap + pos;
-        const uint4* cp = reinterpret_cast<const uint4*>(lat_codes + row * 256 + 128 * hf);
-        const uint4* sp = reinterpret_cast<const uint4*>(lat_scales + row * 32 + 16 * hf);
-        const uint4 sv = __ldg(sp);
-        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {  // 16 code bytes = 32 dims = 2 scale blocks
-          const uint4 cv = __ldg(cp + c8);
-          const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+    for (int hh = 0; hh < 2; ++hh) {
+      const int h = 2 * w + hh;
+      const size_t base = ((size_t)b * H + hg * kAttnHeads + h) * 512 + 16 * lane;
+      float x[16];
+      if (q_dtype == CSA2_F32) {
+        const float4* p4 = reinterpret_cast<const float4*>(static_cast<const float*>(q) + base);
 #pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {   // one 16-dim scale block = 2 chunks of 8 dims
-            const int sidx = 2 * c8 + hb;
-            const float sf = e4m3_decode((sw[sidx >> 2] >> (8 * (sidx & 3))) & 0xFFu);
-            const __half2 s2 = __float2half2_rn(sf);
-            uint32_t o[8];
+        for (int i = 0; i < 4; ++i) {
+          const float4 v = __ldg(p4 + i);
+          x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+        }
+      } else {
+        const uint4* p4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + base);
 #pragma unroll
-            for (int wv = 0; wv < 2; ++wv) {
-              const uint32_t word = cw[2 * hb + wv];
+        for (int i = 0; i < 2; ++i) {
+          const uint4 v = __ldg(p4 + i);
+          const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int by = 0; by < 4; ++by) {
-                const __half2_raw r =
-                    __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((word >> (8 * by)) & 0xFFu), __NV_E2M1);
-                const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&r), s2);
-                o[4 * wv + by] = *reinterpret_cast<const uint32_t*>(&v);
-              }
-            }
-            const int chunk = 32 * hf + 4 * c8 + 2 * hb;
-            *reinterpret_cast<uint4*>(vs + swz(kk, chunk, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(vs + swz(kk, chunk + 1, 64)) = make_uint4(o[4], o[5], o[6], o[7]);
+          for (int j = 0; j < 4; ++j) {
+            x[8 * i + 2 * j] = __uint_as_float(ww[j] << 16);
+            x[8 * i + 2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
           }
         }
       }
-    } else {
-      const int wr = (split - n_idx_splits) * kAttnKeys + kk;
-      ok = wr < W;
-      if (ok) {
-        const uint4* src = reinterpret_cast<const uint4*>(swa + ((size_t)b * W + wr) * 512 + 256 * hf);
-#pragma unroll 4
-        for (int c = 0; c < 32; ++c) {
-          const uint4 v = __ldg(src + c);
-          const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[4];
+      float mx = 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            o[i] = pack_half2(bf16_bits_to_float(vw[i] & 0xFFFFu), bf16_bits_to_float(vw[i] >> 16));
-          *reinterpret_cast<uint4*>(vs + swz(kk, 32 * hf + c, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(x[i]));
+      mx = warp_max(mx);
+      int sq = 0;
+      if (mx > 0.f) {
+        const int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2) for normal mx
+        sq = min(max(14 - e, -100), 100);
+      }
+      const float f = __uint_as_float((uint32_t)(sq + 127) << 23);  // 2^sq, exact
+      if (lane == 0) coef[h] = scale * kLog2e * __uint_as_float((uint32_t)(127 - sq) << 23);
+#pragma unroll
+      for (int part = 0; part < NPART; ++part) {
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float v[2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float y = x[2 * i + j] * f;
+            const float hi = __half2float(__float2half_rn(y));
+            v[j] = part == 0 ? hi : y - hi;
+          }
+          o[i] = pack_half2(v[0], v[1]);
+        }
+        unsigned char* qs = vs + part * (kAttnHeads * 1024);
+        *reinterpret_cast<uint4*>(qs + swz(h, 2 * lane, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(qs + swz(h, 2 * lane + 1, 64)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+  }
+  __syncthreads();
+  uint32_t qf[NPART][8][4];
+#pragma unroll
+  for (int part = 0; part < NPART; ++part) {
+    const uint32_t qb = smem_u32(vs + part * (kAttnHeads * 1024));
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      ldsm_x4(qb + swz(lane & 15, 16 * dg + 2 * ks + (lane >> 4), 64), qf[part][ks][0], qf[part][ks][1],
+              qf[part][ks][2], qf[part][ks][3]);
+  }
+  const float cf0 = coef[g], cf1 = coef[g + 8];
+  __syncthreads();  // the V area is free again
+
+  float oacc[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads g, g+8
+
+  for (int c = 0; c < n_chunks; ++c) {
+    // ---- chunk keys -> fp16 V rows
+    {
+      const int kk = tid >> 2, qq = tid & 3;  // key kk, dims 128qq .. 128qq+127
+      bool ok = false;
+      if (c < n_idx_chunks) {
+        cp_async_wait_all();
+        __syncthreads();
+        const int j = c * kAttnChunk + kk;
+        const int pos = j < k ? __ldg(idxrow + j) : -1;
+        if (pos >= n_b) set_dev_error(CSA2_ERR_BOUNDS);
+        ok = pos >= 0 && pos < n_b;
+        if (ok) {
+          const unsigned char* rc = smem + kAttnRawC + kk * 256 + 64 * qq;
+          const unsigned char* rs = smem + kAttnRawS + kk * 32 + 8 * qq;
+          const uint2 sc8 = *reinterpret_cast<const uint2*>(rs);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {  // 16 code bytes = 32 dims = 2 scale blocks
+            const uint4 cv = *reinterpret_cast<const uint4*>(rc + 16 * i);
+            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              const int sidx = 2 * i + hb;
+              const uint32_t sbyte = ((sidx < 4 ? sc8.x : sc8.y) >> (8 * (sidx & 3))) & 0xFFu;
+              const __half2 s2 = __float2half2_rn(e4m3_decode(sbyte));
+              uint32_t o[8];
+#pragma unroll
+              for (int wv = 0; wv < 2; ++wv) {
+                const uint32_t word = cw[2 * hb + wv];
+#pragma unroll
+                for (int by = 0; by < 4; ++by) {
+                  const __half2_raw r =
+                      __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((word >> (8 * by)) & 0xFFu), __NV_E2M1);
+                  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&r), s2);
+                  o[4 * wv + by] = *reinterpret_cast<const uint32_t*>(&v);
+                }
+              }
+              const int chunk = 16 * qq + 4 * i + 2 * hb;
+              *reinterpret_cast<uint4*>(vs + swz(kk, chunk, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(vs + swz(kk, chunk + 1, 64)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+          }
+        }
+      } else {
+        __syncthreads();
+        const int wr = (c - n_idx_chunks) * kAttnChunk + kk;
+        ok = wr < W;
+        if (ok) {
+          const uint4* src = reinterpret_cast<const uint4*>(swa + ((size_t)b * W + wr) * 512 + 128 * qq);
+#pragma unroll 4
+          for (int i = 0; i < 16; ++i) {
+            const uint4 v = __ldg(src + i);
+            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              o[e] = pack_half2(bf16_bits_to_float(vw[e] & 0xFFFFu), bf16_bits_to_float(vw[e] >> 16));
+            *reinterpret_cast<uint4*>(vs + swz(kk, 16 * qq + i, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+      if (!ok) {
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i)
+          *reinterpret_cast<uint4*>(vs + swz(kk, 16 * qq + i, 64)) = make_uint4(0, 0, 0, 0);
+      }
+      if (qq == 0) key_ok[kk] = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (c + 1 < n_idx_chunks) attn_prefetch_chunk(smem, lat_codes, lat_scales, idxrow, k, c + 1, n_b, seq_row0);
+
+    // ---- S partial = Q V^T over this warp's keys (32kg..) and dims (128dg..)
+    {
+      float sacc[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+      const uint32_t vb = smem_u32(vs);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int key = 32 * kg + 16 * jj + (lane & 7) + ((lane >> 4) << 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(vb + swz(key, 16 * dg + 2 * ks + ((lane >> 3) & 1), 64), b0, b1, b2, b3);
+#pragma unroll
+          for (int part = 0; part < NPART; ++part) {
+            mma_f16(sacc[2 * jj], qf[part][ks][0], qf[part][ks][1], qf[part][ks][2], qf[part][ks][3], b0, b1);
+            mma_f16(sacc[2 * jj + 1], qf[part][ks][0], qf[part][ks][1], qf[part][ks][2], qf[part][ks][3], b2, b3);
+          }
+        }
+      }
+      float* sp = spart + dg * kAttnHeads * kAttnSPitch;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int key = 32 * kg + 8 * j + 2 * t4;
+        *reinterpret_cast<float2*>(sp + g * kAttnSPitch + key) = make_float2(sacc[j][0], sacc[j][1]);
+        *reinterpret_cast<float2*>(sp + (g + 8) * kAttnSPitch + key) = make_float2(sacc[j][2], sacc[j][3]);
+      }
+    }
+    __syncthreads();
+
+    // ---- softmax: warp w finishes keys 8w..8w+7 (heads g, g+8)
+    float alpha0, alpha1;
+    {
+      const int key = 8 * w + 2 * t4;
+      float s[4] = {0.f, 0.f, 0.f, 0.f};  // (g, key), (g, key+1), (g+8, key), (g+8, key+1)
+#pragma unroll
+      for (int d = 0; d < 4; ++d) {
+        const float* sp = spart + d * kAttnHeads * kAttnSPitch;
+        const float2 a = *reinterpret_cast<const float2*>(sp + g * kAttnSPitch + key);
+        const float2 bq = *reinterpret_cast<const float2*>(sp + (g + 8) * kAttnSPitch + key);
+        s[0] += a.x; s[1] += a.y; s[2] += bq.x; s[3] += bq.y;
+      }
+      const bool ok0 = key_ok[key] != 0, ok1 = key_ok[key + 1] != 0;
+      s[0] = ok0 ? s[0] * cf0 : -INFINITY;
+      s[1] = ok1 ? s[1] * cf0 : -INFINITY;
+      s[2] = ok0 ? s[2] * cf1 : -INFINITY;
+      s[3] = ok1 ? s[3] * cf1 : -INFINITY;
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      if (t4 == 0) {
+        red_m[w * kAttnHeads + g] = mx0;
+        red_m[w * kAttnHeads + g + 8] = mx1;
+      }
+      __syncthreads();
+      float M0 = m0, M1 = m1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        M0 = fmaxf(M0, red_m[i * kAttnHeads + g]);
+        M1 = fmaxf(M1, red_m[i * kAttnHeads + g + 8]);
+      }
+      const float Z0 = M0 == -INFINITY ? 0.f : M0, Z1 = M1 == -INFINITY ? 0.f : M1;
+      alpha0 = exp2f(m0 - Z0);  // m = -inf -> 0 (O and l are still 0)
+      alpha1 = exp2f(m1 - Z1);
+      m0 = M0;
+      m1 = M1;
+      const __half2 p01 = __floats2half2_rn(exp2f(s[0] - Z0), exp2f(s[1] - Z0));
+      const __half2 p23 = __floats2half2_rn(exp2f(s[2] - Z1), exp2f(s[3] - Z1));
+      const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
+      float ls0 = f01.x + f01.y, ls1 = f23.x + f23.y;
+      *reinterpret_cast<__half2*>(ps + swz(g, key >> 3, 8) + (key & 7) * 2) = p01;
+      *reinterpret_cast<__half2*>(ps + swz(g + 8, key >> 3, 8) + (key & 7) * 2) = p23;
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, 1);
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, 2);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, 1);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, 2);
+      if (t4 == 0) {
+        red_l[w * kAttnHeads + g] = ls0;
+        red_l[w * kAttnHeads + g + 8] = ls1;
+      }
+      __syncthreads();
+      float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        L0 += red_l[i * kAttnHeads + g];
+        L1 += red_l[i * kAttnHeads + g + 8];
+      }
+      l0 = l0 * alpha0 + L0;
+      l1 = l1 * alpha1 + L1;
+    }
+
+    // ---- O = alpha O + P V (warp w: dims 64w .. 64w+63)
+    {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        oacc[j][0] *= alpha0; oacc[j][1] *= alpha0;
+        oacc[j][2] *= alpha1; oacc[j][3] *= alpha1;
+      }
+      const uint32_t pb = smem_u32(ps), vb = smem_u32(vs);
+#pragma unroll
+      for (int ks = 0; ks < kAttnChunk / 16; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(pb + swz(lane & 15, 2 * ks + (lane >> 4), 8), a0, a1, a2, a3);
+        const int key = 16 * ks + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vb + swz(key, (64 * w + 16 * jj) / 8 + (lane >> 4), 64), b0, b1, b2, b3);
+          mma_f16(oacc[2 * jj], a0, a1, a2, a3, b0, b1);
+          mma_f16(oacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
         }
       }
     }
-    if (!ok) {
-      for (int c = 0; c < 32; ++c)
-        *reinterpret_cast<uint4*>(vs + swz(kk, 32 * hf + c, 64)) = make_uint4(0, 0, 0, 0);
-    }
-    if (hf == 0) key_ok[kk] = ok ? 1 : 0;
-  }
-  __syncthreads();
-
-  // ---- S = Q V^T  (warp: head tile ht, keys [kg*KW, kg*KW + KW))
-  const int ht = wid % HT, kg = wid / HT;
-  float sacc[S::NT1][4];
-#pragma unroll
-  for (int j = 0; j < S::NT1; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
-  const int n_parts = q_dtype == CSA2_F32 ? 2 : 1;
-  for (int part = 0; part < n_parts; ++part) {
-    __syncthreads();
-    attn_load_q<H>(q, q_dtype, b, sq_pow, qs, part);
-    __syncthreads();
-    const uint32_t qb = smem_u32(qs), vb = smem_u32(vs);
-#pragma unroll 2
-    for (int ks = 0; ks < 32; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(qb + swz(ht * 16 + (lane & 15), 2 * ks + (lane >> 4), 64), a0, a1, a2, a3);
-#pragma unroll
-      for (int jj = 0; jj < S::NT1 / 2; ++jj) {
-        const int key = kg * S::KW + 16 * jj + (lane & 7) + ((lane >> 4) << 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(vb + swz(key, 2 * ks + ((lane >> 3) & 1), 64), b0, b1, b2, b3);
-        mma_f16(sacc[2 * jj], a0, a1, a2, a3, b0, b1);
-        mma_f16(sacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
-      }
-    }
   }
 
-  // ---- softmax over this split's keys (base-2 logits)
-  const int h0 = ht * 16 + g, h1 = h0 + 8;
-  const float c0 = scale * kLog2e / sq_pow[h0], c1 = scale * kLog2e / sq_pow[h1];
-  float mx0 = -INFINITY, mx1 = -INFINITY;
+  // ---- normalise and store
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  float* o0 = out + ((size_t)b * H + hg * kAttnHeads + g) * 512;
+  float* o1 = o0 + 8 * 512;
 #pragma unroll
-  for (int j = 0; j < S::NT1; ++j) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int key = kg * S::KW + 8 * j + 2 * t4 + e;
-      const bool okk = key_ok[key] != 0;
-      sacc[j][e] = okk ? sacc[j][e] * c0 : -INFINITY;
-      sacc[j][2 + e] = okk ? sacc[j][2 + e] * c1 : -INFINITY;
-      mx0 = fmaxf(mx0, sacc[j][e]);
-      mx1 = fmaxf(mx1, sacc[j][2 + e]);
-    }
+  for (int j = 0; j < 8; ++j) {
+    const int d = 64 * w + 8 * j + 2 * t4;
+    *reinterpret_cast<float2*>(o0 + d) = make_float2(oacc[j][0] * inv0, oacc[j][1] * inv0);
+    *reinterpret_cast<float2*>(o1 + d) = make_float2(oacc[j][2] * inv1, oacc[j][3] * inv1);
   }
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-  if (t4 == 0) { red_m[kg * H + h0] = mx0; red_m[kg * H + h1] = mx1; }
-  __syncthreads();
-  float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < S::NKG; ++i) { M0 = fmaxf(M0, red_m[i * H + h0]); M1 = fmaxf(M1, red_m[i * H + h1]); }
-  const float Z0 = M0 == -INFINITY ? 0.f : M0, Z1 = M1 == -INFINITY ? 0.f : M1;
-  float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-  for (int j = 0; j < S::NT1; ++j) {
-    const __half2 p01 = __floats2half2_rn(exp2f(sacc[j][0] - Z0), exp2f(sacc[j][1] - Z0));
-    const __half2 p23 = __floats2half2_rn(exp2f(sacc[j][2] - Z1), exp2f(sacc[j][3] - Z1));
-    const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
-    l0 += f01.x + f01.y;
-    l1 += f23.x + f23.y;
-    const int key = kg * S::KW + 8 * j + 2 * t4;  // chunk key/8, element key%8
-    *reinterpret_cast<__half2*>(ps + swz(h0, key >> 3, 16) + (key & 7) * 2) = p01;
-    *reinterpret_cast<__half2*>(ps + swz(h1, key >> 3, 16) + (key & 7) * 2) = p23;
-  }
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  if (t4 == 0) { red_l[kg * H + h0] = l0; red_l[kg * H + h1] = l1; }
-  __syncthreads();
-
-  // ---- O = P V  (warp: head tile ht, dims [dg*DW, dg*DW + DW))
-  const int dg = wid / HT;
-  float oacc[S::NT2][4];
-#pragma unroll
-  for (int j = 0; j < S::NT2; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
-  {
-    const uint32_t pb = smem_u32(ps), vb = smem_u32(vs);
-#pragma unroll
-    for (int ks = 0; ks < kAttnKeys / 16; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(pb + swz(ht * 16 + (lane & 15), 2 * ks + (lane >> 4), 16), a0, a1, a2, a3);
-      const int key = 16 * ks + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-      for (int jj = 0; jj < S::NT2 / 2; ++jj) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + swz(key, (dg * S::DW + 16 * jj) / 8 + (lane >> 4), 64), b0, b1, b2, b3);
-        mma_f16(oacc[2 * jj], a0, a1, a2, a3, b0, b1);
-        mma_f16(oacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
-      }
-    }
-  }
-
-  // ---- partial results
-  const size_t pbase = ((size_t)b * n_splits + split) * H;
-  float* o0 = part_o + (pbase + h0) * 512;
-  float* o1 = part_o + (pbase + h1) * 512;
-#pragma unroll
-  for (int j = 0; j < S::NT2; ++j) {
-    const int d = dg * S::DW + 8 * j + 2 * t4;
-    *reinterpret_cast<float2*>(o0 + d) = make_float2(oacc[j][0], oacc[j][1]);
-    *reinterpret_cast<float2*>(o1 + d) = make_float2(oacc[j][2], oacc[j][3]);
-  }
-  if (dg == 0 && t4 == 0) {
-    float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-    for (int i = 0; i < S::NKG; ++i) { L0 += red_l[i * H + h0]; L1 += red_l[i * H + h1]; }
-    part_ml[(pbase + h0) * 2] = M0;
-    part_ml[(pbase + h0) * 2 + 1] = L0;
-    part_ml[(pbase + h1) * 2] = M1;
-    part_ml[(pbase + h1) * 2 + 1] = L1;
-  }
-}
-
-// Merge the split partials: o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
-__global__ void __launch_bounds__(128)
-k_attn_combine(const float* __restrict__ part_o, const float* __restrict__ part_ml, int n_splits,
-               int H, float* __restrict__ out) {
-  const int b = blockIdx.y, h = blockIdx.x;
-  float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, part_ml[(((size_t)b * n_splits + s) * H + h) * 2]);
-  float L = 0.f;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  if (M != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const size_t ph = ((size_t)b * n_splits + s) * H + h;
-      const float m = part_ml[ph * 2];
-      if (m == -INFINITY) continue;
-      const float wgt = exp2f(m - M);
-      L += wgt * part_ml[ph * 2 + 1];
-      const float4 v = *reinterpret_cast<const float4*>(part_o + ph * 512 + 4 * threadIdx.x);
-      acc[0] += wgt * v.x; acc[1] += wgt * v.y; acc[2] += wgt * v.z; acc[3] += wgt * v.w;
-    }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  *reinterpret_cast<float4*>(out + ((size_t)b * H + h) * 512 + 4 * threadIdx.x) =
-      make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
 }
 
 }  // namespace csa2

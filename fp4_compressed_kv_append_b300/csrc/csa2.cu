@@ -36,11 +36,13 @@ csa2_status check_cache(const csa2_cache_view* c) {
   return CSA2_OK;
 }
 
-inline int attn_splits(int k, int W) { return (k + kAttnKeys - 1) / kAttnKeys + (W + kAttnKeys - 1) / kAttnKeys; }
-
+// sparse_latent_attn keeps its partial results on chip: it needs no scratch.
 size_t attn_ws_bytes(int batch, int H, int k, int W) {
-  const size_t s = (size_t)attn_splits(k, W);
-  return round_up(s * batch * H * 512 * sizeof(float), 256) + round_up(s * batch * H * 2 * sizeof(float), 256);
+  (void)batch;
+  (void)H;
+  (void)k;
+  (void)W;
+  return 0;
 }
 
 // ------------------------------------------------------------ launchers (no validation)
@@ -127,7 +129,7 @@ void launch_scan_tma(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s)
     cudaFuncSetAttribute(k_indexer_scan_tma<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem);
     attr_set = true;
   }
-  const int64_t full = (int64_t)sm_count() * 2;
+  const int64_t full = (int64_t)sm_count() * 3;
   const int grid = (int)(a.total_tiles < full ? a.total_tiles : full);
   k_indexer_scan_tma<NPART><<<grid, kTmaThreads, kTmaSmem, s>>>(m, a);
 }
@@ -176,44 +178,30 @@ void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, c
   static bool attr_set = false;
   if (!attr_set) {
     cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)(sizeof(TopkCtl) + 8u * topk_cap(CSA2_MAX_TOPK)));
+                         (int)topk_smem_bytes(CSA2_MAX_TOPK));
     attr_set = true;
   }
-  const size_t smem = sizeof(TopkCtl) + 8u * topk_cap(k);
-  k_topk<<<batch, kTopkThreads, smem, s>>>(scores, stride, n, cand, k, out);
+  k_topk<<<dim3(kTopkCluster, batch), kTopkThreads, topk_smem_bytes(k), s>>>(scores, stride, n, cand, k, out);
   g_launches += 1;
 }
 
-template <int HT>
-void launch_attn_t(const void* q, csa2_dtype dt, float scale, const csa2_cache_view& c, const int32_t* idx, int k,
-                   const uint16_t* swa, int W, int n_idx_splits, int n_splits, float* part_o, float* part_ml,
-                   cudaStream_t s) {
+template <int NPART>
+void launch_attn_t(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
+                   int k, const uint16_t* swa, int W, float* out, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(k_sparse_attn_mma<HT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)AttnShape<HT>::smem);
+    cudaFuncSetAttribute(k_sparse_attn<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
     attr_set = true;
   }
-  k_sparse_attn_mma<HT><<<dim3(n_splits, c.batch), kAttnThreads, AttnShape<HT>::smem, s>>>(
-      q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, n_idx_splits, part_o,
-      part_ml);
+  k_sparse_attn<NPART><<<dim3(H / kAttnHeads, c.batch), kAttnThreads, kAttnSmem, s>>>(
+      q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H, out);
 }
 
 void launch_attn(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
                  int k, const uint16_t* swa, int W, float* out, void* ws, cudaStream_t s) {
-  const int n_idx_splits = (k + kAttnKeys - 1) / kAttnKeys;
-  const int n_splits = attn_splits(k, W);
-  const size_t s_count = (size_t)n_splits;
-  float* part_o = static_cast<float*>(ws);
-  float* part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                            round_up(s_count * c.batch * H * 512 * sizeof(float), 256));
-  if (n_splits > 0) {
-    if (H == 16) launch_attn_t<1>(q, dt, scale, c, idx, k, swa, W, n_idx_splits, n_splits, part_o, part_ml, s);
-    else if (H == 32) launch_attn_t<2>(q, dt, scale, c, idx, k, swa, W, n_idx_splits, n_splits, part_o, part_ml, s);
-    else launch_attn_t<4>(q, dt, scale, c, idx, k, swa, W, n_idx_splits, n_splits, part_o, part_ml, s);
-    g_launches += 1;
-  }
-  k_attn_combine<<<dim3(H, c.batch), 128, 0, s>>>(part_o, part_ml, n_splits, H, out);
+  (void)ws;
+  if (dt == CSA2_F32) launch_attn_t<2>(q, dt, H, scale, c, idx, k, swa, W, out, s);
+  else launch_attn_t<1>(q, dt, H, scale, c, idx, k, swa, W, out, s);
   g_launches += 1;
 }
 
@@ -271,8 +259,8 @@ csa2_status sparse_latent_attn(const void* q, csa2_dtype q_dtype, int32_t H, flo
   if (!(scale > 0.f) || k < 0 || k > CSA2_MAX_TOPK || W < 0 || W > CSA2_MAX_WINDOW) return CSA2_ERR_ARG;
   if ((k > 0 && !idx) || (W > 0 && !swa)) return CSA2_ERR_ARG;
   if (!aligned16(q) || !aligned16(out) || (W > 0 && !aligned16(swa))) return CSA2_ERR_ALIGN;
-  if (!ws || ws_bytes < attn_ws_bytes(cache->batch, H, k, W)) return CSA2_ERR_WORKSPACE;
-  if (!aligned16(ws)) return CSA2_ERR_ALIGN;
+  (void)ws;
+  (void)ws_bytes;
   launch_attn(q, q_dtype, H, scale, *cache, idx, k, swa, W, out, ws, (cudaStream_t)stream);
   return launch_status();
 }

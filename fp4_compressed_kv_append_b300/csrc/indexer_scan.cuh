@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan_gather(const S
 // Scores every entry of every sequence. A producer warp streams 128-entry tiles
 // of codes (one TMA box of 128 rows x 64 bytes, 64-byte swizzle) and their E8M0
 // bytes (one 512-byte bulk copy) into a ring of shared-memory stages; eight
-// consumer warps take 16 rows each per stage. Full/empty mbarriers hand the
+// consumer warps take 16 rows each per stage. Three blocks share an SM. Full/empty mbarriers hand the
 // stages back and forth; every wait gives up after about a second, records
 // CSA2_ERR_TIMEOUT and stops the block.
 //
@@ -392,7 +392,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 template <int NPART>
-__global__ void __launch_bounds__(kTmaThreads, 2)
+__global__ void __launch_bounds__(kTmaThreads, 3)
 k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(

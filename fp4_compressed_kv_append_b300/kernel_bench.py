@@ -5,9 +5,9 @@
 
 Kernels: scan (indexer_score over every entry), topk (topk_select, k = 512),
 attn (sparse_latent_attn over 512 selected entries), append (kv_quant_append of
-one token per sequence), step (one Full-layer csa2_decode_step). Each launch is
-timed with CUDA events on the launching stream; with --flush a 256 MB buffer is
-written between launches so that L2 holds nothing of the inputs. Prints one JSON
+one token per sequence), step (one Full-layer csa2_decode_step). The launches are
+captured in a CUDA graph, each between two CUDA events; with --flush a 256 MB
+buffer is written between launches so that L2 holds nothing of the inputs. Prints one JSON
 line per kernel: average microseconds per launch, algorithmic bytes per launch
 (68 per scanned entry, 288 per gathered entry, 4 per score read by Top-k) and
 the resulting GB/s.
@@ -38,17 +38,26 @@ def make_cache(B, N, seed=0):
 
 
 def time_launches(fn, iters, warmup, flush):
+    """Average device time of fn's launches. The launches are captured in a CUDA
+    graph with an event pair around each one, so host-side submission time is
+    not counted."""
     buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush else None
     for _ in range(warmup):
         fn()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
     torch.cuda.synchronize()
-    for a, b in ev:
-        if buf is not None:
-            buf.fill_(1)
-        a.record()
-        fn()
-        b.record()
+    ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+          for _ in range(iters)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for a, b in ev:
+            if buf is not None:
+                buf.fill_(1)
+            a.record()
+            fn()
+            b.record()
+    g.replay()  # warm
+    torch.cuda.synchronize()
+    g.replay()
     torch.cuda.synchronize()
     return sum(a.elapsed_time(b) for a, b in ev) / iters * 1e3
 

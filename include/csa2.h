@@ -151,11 +151,13 @@ CSA2_API csa2_status topk_select(const float* scores, const int32_t* n, int64_t 
  * window rows together, o_h = sum_j p_hj v_j, written in float32.
  *   q [batch][H][512] (q_dtype), H in {16, 32, 64}; scale > 0 (1/sqrt(512)).
  *   cache: the main KV (only lat_codes/lat_scales/len/cap are read).
- *   idx [batch][k] positions, -1 skipped; 0 <= k <= CSA2_MAX_TOPK.
+ *   idx [batch][k] positions, -1 skipped; 0 <= k <= CSA2_MAX_TOPK. A position
+ *     >= len[b] is skipped and records CSA2_ERR_BOUNDS.
  *   swa [batch][W][512] bf16 window rows ("La contrepartie : la fenetre
  *     glissante"; "Troisiemement": 128 tokens), NULL with W = 0.
  *   out [batch][H][512] f32. With no key at all the output row is zero.
- *   ws/ws_bytes: scratch, at least csa2_attn_workspace_size(batch, H, k, W).
+ *   ws/ws_bytes: scratch; csa2_attn_workspace_size() is 0 for every shape (the
+ *     partial results stay on chip), so ws may be NULL.
  */
 CSA2_API csa2_status sparse_latent_attn(const void* q, csa2_dtype q_dtype, int32_t H, float scale,
                                const csa2_cache_view* cache /* host struct */,
@@ -205,7 +207,8 @@ CSA2_API csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_l
 /* Scratch bytes of csa2_decode_step for these sizes (max_entries = cap). */
 CSA2_API size_t csa2_workspace_size(int32_t batch, int64_t max_entries, int32_t H, int32_t k, int32_t pool,
                            int32_t W);
-/* Scratch bytes of topk_select / sparse_latent_attn. */
+/* Scratch bytes of topk_select / sparse_latent_attn (both 0: they keep their state
+ * in shared memory; the arguments are kept for callers that size buffers). */
 CSA2_API size_t csa2_topk_workspace_size(int32_t batch, int64_t stride, int32_t k);
 CSA2_API size_t csa2_attn_workspace_size(int32_t batch, int32_t H, int32_t k, int32_t W);
 

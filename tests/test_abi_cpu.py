@@ -37,11 +37,15 @@ def test_status_strings():
 
 def test_workspace_sizes():
     L = A.lib()
-    # 4 splits of 128 keys for k = 512; partial o and (m, l) per split, rounded to 256 B
-    assert L.csa2_attn_workspace_size(32, 64, 512, 0) == 4 * 32 * 64 * 512 * 4 + 4 * 32 * 64 * 2 * 4
-    assert L.csa2_attn_workspace_size(1, 16, 512, 128) == 5 * 16 * 512 * 4 + 768
+    # attention and Top-k keep their state on chip
+    assert L.csa2_attn_workspace_size(32, 64, 512, 0) == 0
+    assert L.csa2_attn_workspace_size(1, 16, 512, 128) == 0
+    assert L.csa2_topk_workspace_size(32, 131072, 512) == 0
+    # the decode step needs the scores, the pool and the selection
     total = L.csa2_workspace_size(32, 131072, 64, 512, 0, 0)
-    assert total >= 32 * 131072 * 4 + 32 * 512 * 4 + L.csa2_attn_workspace_size(32, 64, 512, 0)
+    assert total >= 32 * 131072 * 4 + 32 * 512 * 4
+    pooled = L.csa2_workspace_size(8, 524288, 64, 512, 16384, 0)
+    assert pooled >= 8 * 524288 * 4 + 2 * 8 * 16384 * 4 + 8 * 512 * 4
 
 
 def _fake_cache(cap=256, batch=2, base=0x10000):
@@ -71,8 +75,6 @@ def test_host_validation_rejects_before_any_launch():
     # attention: head count, workspace
     assert L.sparse_latent_attn(0x100, A.BF16, 48, 0.04, C.byref(cv), 0x200, 512, None, 0, 0x300, 0x400,
                                 1 << 30, None) == A.ERR_UNSUPPORTED
-    assert L.sparse_latent_attn(0x100, A.BF16, 64, 0.04, C.byref(cv), 0x200, 512, None, 0, 0x300, 0x400, 16,
-                                None) == A.ERR_WORKSPACE
     assert L.sparse_latent_attn(0x100, A.BF16, 64, 0.04, C.byref(cv), 0x200, 512, None, 5, 0x300, 0x400,
                                 1 << 30, None) == A.ERR_ARG
 
