@@ -6,9 +6,11 @@
 // token", "Troisiemement" (E2M1 values with an E4M3 scale per 16 channels; a
 // 128-token sliding window kept outside the global cache).
 //
-// One 256-thread block per (sequence, group of 16 heads) walks all selected keys,
-// then the window rows, in chunks of 64 with an online softmax -- no partial
-// results leave the block. Per chunk:
+// A cluster of two 256-thread blocks per (sequence, group of 16 heads) walks the
+// selected keys, then the window rows, in chunks of 64 with an online softmax,
+// block r taking half r of the chunks; block 1 then hands its (max, sum, O) to
+// block 0 through distributed shared memory and block 0 writes the merged
+// result -- nothing partial goes through global memory. Per chunk:
 //  * the raw codes and scales of the chunk's entries were gathered into shared
 //    memory by cp.async during the previous chunk; they are dequantised to fp16
 //    (exact: an E2M1 value times an E4M3 scale has at most 6 significant bits and
@@ -24,6 +26,8 @@
 // the logit coefficient.
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace csa2 {
@@ -35,8 +39,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // shared-memory layout (bytes)
 constexpr int kAttnV = 0;                                     // [64 keys][512] fp16, swizzled; Q first
-constexpr int kAttnRawC = kAttnV + kAttnChunk * 1024;         // [64][256] codes
-constexpr int kAttnRawS = kAttnRawC + kAttnChunk * 256;       // [64][32] E4M3 scales
+constexpr int kAttnRawPitch = 272;                           // bytes per raw code row (padded)
+constexpr int kAttnRawC = kAttnV + kAttnChunk * 1024;         // [64][272] codes
+constexpr int kAttnRawS = kAttnRawC + kAttnChunk * kAttnRawPitch;  // [64][32] E4M3 scales
 constexpr int kAttnSPitch = 68;                               // floats per S-partial row
 constexpr int kAttnSPart = kAttnRawS + kAttnChunk * 32;       // [4 dg][16 heads][68] f32
 constexpr int kAttnP = kAttnSPart + 4 * kAttnHeads * kAttnSPitch * 4;  // [16][64] fp16, swizzled
@@ -44,10 +49,20 @@ constexpr int kAttnRedM = kAttnP + kAttnHeads * 128;          // [8 warps][16] f
 constexpr int kAttnRedL = kAttnRedM + 8 * kAttnHeads * 4;     // [8 warps][16] f32
 constexpr int kAttnCoef = kAttnRedL + 8 * kAttnHeads * 4;     // [16] f32
 constexpr int kAttnKeyOk = kAttnCoef + kAttnHeads * 4;        // [64] i32
+constexpr int kAttnXO = kAttnV;                              // partner partials: [32][256] f32 (end)
+constexpr int kAttnXML = kAttnSPart;                          // partner m, l per head: [2][16] f32
 constexpr int kAttnSmem = kAttnKeyOk + kAttnChunk * 4;
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk, int chunks_per_row) {
   return (uint32_t)(row * chunks_per_row * 16 + ((chunk ^ (row & 7)) << 4));
+}
+
+// 16-byte chunk c of a 1024-byte row (keys, or query heads): the chunk index is
+// XORed with the row (8 consecutive rows of one chunk column hit 8 bank groups,
+// as ldmatrix reads them) and with its own bits 4-5 (the four threads that
+// dequantise chunks c, c+16, c+32, c+48 of one row hit 4 bank groups).
+__device__ __forceinline__ uint32_t swzv(int row, int chunk) {
+  return (uint32_t)(row * 1024 + ((chunk ^ (row & 7) ^ ((chunk >> 4) & 3)) << 4));
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -94,7 +109,7 @@ __device__ __forceinline__ void attn_prefetch_chunk(unsigned char* smem, const u
     const int pos = j < k ? __ldg(idxrow + j) : -1;
     if (pos >= 0 && pos < n_b) {
       const uint8_t* src = lat_codes + (seq_row0 + pos) * 256 + 64 * part;
-      const uint32_t dst = smem_u32(smem + kAttnRawC + kk * 256 + 64 * part);
+      const uint32_t dst = smem_u32(smem + kAttnRawC + kk * kAttnRawPitch + 64 * part);
 #pragma unroll
       for (int i = 0; i < 4; ++i) cp_async16(dst + 16 * i, src + 16 * i);
     }
@@ -110,7 +125,7 @@ __device__ __forceinline__ void attn_prefetch_chunk(unsigned char* smem, const u
 }
 
 template <int NPART>
-__global__ void __launch_bounds__(kAttnThreads, NPART == 1 ? 2 : 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, NPART == 1 ? 2 : 1)
 k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_t* __restrict__ lat_codes,
               const uint8_t* __restrict__ lat_scales, const int32_t* __restrict__ len, int64_t cap,
               const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int W, int H,
@@ -124,7 +139,10 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
   float* coef = reinterpret_cast<float*>(smem + kAttnCoef);
   int* key_ok = reinterpret_cast<int*>(smem + kAttnKeyOk);
 
-  const int hg = blockIdx.x, b = blockIdx.y;
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int half = (int)cluster.block_rank();  // 0 or 1: which half of the chunks
+  const int hg = blockIdx.x >> 1, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
   const int kg = w & 1, dg = w >> 1;
@@ -133,8 +151,11 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
   const int32_t* idxrow = idx ? idx + (size_t)b * k : nullptr;
   const int n_idx_chunks = (k + kAttnChunk - 1) / kAttnChunk;
   const int n_chunks = n_idx_chunks + (W + kAttnChunk - 1) / kAttnChunk;
+  const int c_begin = half == 0 ? 0 : (n_chunks + 1) / 2;
+  const int c_end = half == 0 ? (n_chunks + 1) / 2 : n_chunks;
 
-  if (n_idx_chunks > 0) attn_prefetch_chunk(smem, lat_codes, lat_scales, idxrow, k, 0, n_b, seq_row0);
+  if (c_begin < n_idx_chunks && c_begin < c_end)
+    attn_prefetch_chunk(smem, lat_codes, lat_scales, idxrow, k, c_begin, n_b, seq_row0);
 
   // ---- queries: per-head 2^s, fp16 parts into the V area, then register fragments
   {
@@ -189,8 +210,8 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
           o[i] = pack_half2(v[0], v[1]);
         }
         unsigned char* qs = vs + part * (kAttnHeads * 1024);
-        *reinterpret_cast<uint4*>(qs + swz(h, 2 * lane, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(qs + swz(h, 2 * lane + 1, 64)) = make_uint4(o[4], o[5], o[6], o[7]);
+        *reinterpret_cast<uint4*>(qs + swzv(h, 2 * lane)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(qs + swzv(h, 2 * lane + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
     }
   }
@@ -201,7 +222,7 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
     const uint32_t qb = smem_u32(vs + part * (kAttnHeads * 1024));
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
-      ldsm_x4(qb + swz(lane & 15, 16 * dg + 2 * ks + (lane >> 4), 64), qf[part][ks][0], qf[part][ks][1],
+      ldsm_x4(qb + swzv(lane & 15, 16 * dg + 2 * ks + (lane >> 4)), qf[part][ks][0], qf[part][ks][1],
               qf[part][ks][2], qf[part][ks][3]);
   }
   const float cf0 = coef[g], cf1 = coef[g + 8];
@@ -212,7 +233,7 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
   for (int j = 0; j < 8; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads g, g+8
 
-  for (int c = 0; c < n_chunks; ++c) {
+  for (int c = c_begin; c < c_end; ++c) {
     // ---- chunk keys -> fp16 V rows
     {
       const int kk = tid >> 2, qq = tid & 3;  // key kk, dims 128qq .. 128qq+127
@@ -225,11 +246,12 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
         if (pos >= n_b) set_dev_error(CSA2_ERR_BOUNDS);
         ok = pos >= 0 && pos < n_b;
         if (ok) {
-          const unsigned char* rc = smem + kAttnRawC + kk * 256 + 64 * qq;
+          const unsigned char* rc = smem + kAttnRawC + kk * kAttnRawPitch + 64 * qq;
           const unsigned char* rs = smem + kAttnRawS + kk * 32 + 8 * qq;
           const uint2 sc8 = *reinterpret_cast<const uint2*>(rs);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {  // 16 code bytes = 32 dims = 2 scale blocks
+          for (int i0 = 0; i0 < 4; ++i0) {  // 16 code bytes = 32 dims = 2 scale blocks
+            const int i = (i0 + qq) & 3;     // rotated: the four threads of a row read distinct banks
             const uint4 cv = *reinterpret_cast<const uint4*>(rc + 16 * i);
             const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
@@ -250,8 +272,8 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
                 }
               }
               const int chunk = 16 * qq + 4 * i + 2 * hb;
-              *reinterpret_cast<uint4*>(vs + swz(kk, chunk, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<uint4*>(vs + swz(kk, chunk + 1, 64)) = make_uint4(o[4], o[5], o[6], o[7]);
+              *reinterpret_cast<uint4*>(vs + swzv(kk, chunk)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(vs + swzv(kk, chunk + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
             }
           }
         }
@@ -269,19 +291,20 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               o[e] = pack_half2(bf16_bits_to_float(vw[e] & 0xFFFFu), bf16_bits_to_float(vw[e] >> 16));
-            *reinterpret_cast<uint4*>(vs + swz(kk, 16 * qq + i, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(vs + swzv(kk, 16 * qq + i)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
       }
       if (!ok) {
 #pragma unroll 4
         for (int i = 0; i < 16; ++i)
-          *reinterpret_cast<uint4*>(vs + swz(kk, 16 * qq + i, 64)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vs + swzv(kk, 16 * qq + i)) = make_uint4(0, 0, 0, 0);
       }
       if (qq == 0) key_ok[kk] = ok ? 1 : 0;
     }
     __syncthreads();
-    if (c + 1 < n_idx_chunks) attn_prefetch_chunk(smem, lat_codes, lat_scales, idxrow, k, c + 1, n_b, seq_row0);
+    if (c + 1 < n_idx_chunks && c + 1 < c_end)
+      attn_prefetch_chunk(smem, lat_codes, lat_scales, idxrow, k, c + 1, n_b, seq_row0);
 
     // ---- S partial = Q V^T over this warp's keys (32kg..) and dims (128dg..)
     {
@@ -295,7 +318,7 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
         for (int jj = 0; jj < 2; ++jj) {
           const int key = 32 * kg + 16 * jj + (lane & 7) + ((lane >> 4) << 3);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(vb + swz(key, 16 * dg + 2 * ks + ((lane >> 3) & 1), 64), b0, b1, b2, b3);
+          ldsm_x4(vb + swzv(key, 16 * dg + 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
 #pragma unroll
           for (int part = 0; part < NPART; ++part) {
             mma_f16(sacc[2 * jj], qf[part][ks][0], qf[part][ks][1], qf[part][ks][2], qf[part][ks][3], b0, b1);
@@ -392,7 +415,7 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vb + swz(key, (64 * w + 16 * jj) / 8 + (lane >> 4), 64), b0, b1, b2, b3);
+          ldsm_x4_t(vb + swzv(key, (64 * w + 16 * jj) / 8 + (lane >> 4)), b0, b1, b2, b3);
           mma_f16(oacc[2 * jj], a0, a1, a2, a3, b0, b1);
           mma_f16(oacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
         }
@@ -400,15 +423,43 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
     }
   }
 
-  // ---- normalise and store
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  float* o0 = out + ((size_t)b * H + hg * kAttnHeads + g) * 512;
-  float* o1 = o0 + 8 * 512;
+  // ---- merge the two halves (block 1 hands (m, l, O) to block 0), normalise, store
+  cluster.sync();  // both halves are done with their shared memory
+  float* xo = cluster.map_shared_rank(reinterpret_cast<float*>(smem + kAttnXO), 0);
+  float* xml = cluster.map_shared_rank(reinterpret_cast<float*>(smem + kAttnXML), 0);
+  if (half == 1) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int d = 64 * w + 8 * j + 2 * t4;
-    *reinterpret_cast<float2*>(o0 + d) = make_float2(oacc[j][0] * inv0, oacc[j][1] * inv0);
-    *reinterpret_cast<float2*>(o1 + d) = make_float2(oacc[j][2] * inv1, oacc[j][3] * inv1);
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) xo[(4 * j + e) * kAttnThreads + tid] = oacc[j][e];
+    if (w == 0 && t4 == 0) {
+      xml[g] = m0;
+      xml[g + 8] = m1;
+      xml[16 + g] = l0;
+      xml[16 + g + 8] = l1;
+    }
+  }
+  cluster.sync();  // no block touches the other's shared memory after this point
+  if (half == 1) return;
+  {
+    const float pm0 = xml[g], pm1 = xml[g + 8], pl0 = xml[16 + g], pl1 = xml[16 + g + 8];
+    const float M0 = fmaxf(m0, pm0), M1 = fmaxf(m1, pm1);
+    const float Z0 = M0 == -INFINITY ? 0.f : M0, Z1 = M1 == -INFINITY ? 0.f : M1;
+    const float a0 = exp2f(m0 - Z0), b0 = exp2f(pm0 - Z0), a1 = exp2f(m1 - Z1), b1 = exp2f(pm1 - Z1);
+    const float L0 = l0 * a0 + pl0 * b0, L1 = l1 * a1 + pl1 * b1;
+    const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
+    float* o0 = out + ((size_t)b * H + hg * kAttnHeads + g) * 512;
+    float* o1 = o0 + 8 * 512;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int d = 64 * w + 8 * j + 2 * t4;
+      const float x0 = (oacc[j][0] * a0 + xo[(4 * j + 0) * kAttnThreads + tid] * b0) * inv0;
+      const float x1 = (oacc[j][1] * a0 + xo[(4 * j + 1) * kAttnThreads + tid] * b0) * inv0;
+      const float x2 = (oacc[j][2] * a1 + xo[(4 * j + 2) * kAttnThreads + tid] * b1) * inv1;
+      const float x3 = (oacc[j][3] * a1 + xo[(4 * j + 3) * kAttnThreads + tid] * b1) * inv1;
+      *reinterpret_cast<float2*>(o0 + d) = make_float2(x0, x1);
+      *reinterpret_cast<float2*>(o1 + d) = make_float2(x2, x3);
+    }
   }
 }
 

@@ -59,8 +59,11 @@ void launch_append(const void* lat, const void* ikey, csa2_dtype dt, int T, int 
     k_quant_append<uint16_t><<<grid, kAppendWarps * 32, 0, s>>>(
         (const uint16_t*)lat, (const uint16_t*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes,
         c.lat_scales, c.idx_codes, c.idx_scales, c.len, c.cap, n_new);
-  k_bump_len<<<(c.batch + 255) / 256, 256, 0, s>>>(c.len, c.batch, c.cap, n_new);
-  g_launches += 2;
+  g_launches += 1;
+  if (grid.x > 1) {  // several blocks per sequence: advance len once they are all done
+    k_bump_len<<<(c.batch + 255) / 256, 256, 0, s>>>(c.len, c.batch, c.cap, n_new);
+    g_launches += 1;
+  }
 }
 
 // Streaming multiprocessors of the current device (cached per device).
@@ -193,7 +196,7 @@ void launch_attn_t(const void* q, csa2_dtype dt, int H, float scale, const csa2_
     cudaFuncSetAttribute(k_sparse_attn<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
     attr_set = true;
   }
-  k_sparse_attn<NPART><<<dim3(H / kAttnHeads, c.batch), kAttnThreads, kAttnSmem, s>>>(
+  k_sparse_attn<NPART><<<dim3(2 * (H / kAttnHeads), c.batch), kAttnThreads, kAttnSmem, s>>>(
       q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H, out);
 }
 

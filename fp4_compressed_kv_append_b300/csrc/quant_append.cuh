@@ -18,23 +18,15 @@ namespace csa2 {
 
 constexpr int kAppendWarps = 8;
 
+// One entry: ratio-2 merge (optional), then both packings. Lane l of the warp.
 template <typename Tin>
-__global__ void __launch_bounds__(kAppendWarps * 32)
-k_quant_append(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T, int ratio,
-               const float* __restrict__ w0l, const float* __restrict__ w1l,
-               const float* __restrict__ w0i, const float* __restrict__ w1i,
-               uint8_t* __restrict__ lat_codes, uint8_t* __restrict__ lat_scales,
-               uint8_t* __restrict__ idx_codes, uint8_t* __restrict__ idx_scales,
-               const int32_t* __restrict__ len, int64_t cap, int n_new) {
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
-  const int b = blockIdx.y;
-  if (e >= n_new) return;
-  const int64_t base = __ldg(len + b);
-  if (base < 0 || base + n_new > cap) {  // the whole append of this sequence is refused
-    if (e == 0 && lane == 0) set_dev_error(CSA2_ERR_BOUNDS);
-    return;
-  }
+__device__ __forceinline__ void quant_append_entry(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
+                                                   int ratio, const float* __restrict__ w0l,
+                                                   const float* __restrict__ w1l, const float* __restrict__ w0i,
+                                                   const float* __restrict__ w1i, uint8_t* __restrict__ lat_codes,
+                                                   uint8_t* __restrict__ lat_scales, uint8_t* __restrict__ idx_codes,
+                                                   uint8_t* __restrict__ idx_scales, int64_t cap, int b, int64_t base,
+                                                   int e, int lane) {
   const int64_t slot = (size_t)b * cap + base + e;
   const size_t tok = (size_t)b * T + (size_t)e * ratio;
 
@@ -104,6 +96,29 @@ k_quant_append(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
   for (int i = 0; i < 4; ++i) kc |= e2m1_encode(z[i] * inv) << (4 * i);
   *reinterpret_cast<uint16_t*>(idx_codes + slot * 64 + 2 * lane) = (uint16_t)kc;
   if ((lane & 7) == 0) idx_scales[slot * 4 + (lane >> 3)] = (uint8_t)(X + 127);
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kAppendWarps * 32)
+k_quant_append(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T, int ratio,
+               const float* __restrict__ w0l, const float* __restrict__ w1l,
+               const float* __restrict__ w0i, const float* __restrict__ w1i,
+               uint8_t* __restrict__ lat_codes, uint8_t* __restrict__ lat_scales,
+               uint8_t* __restrict__ idx_codes, uint8_t* __restrict__ idx_scales,
+               int32_t* __restrict__ len, int64_t cap, int n_new) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+  const int b = blockIdx.y;
+  const int64_t base = len[b];
+  const bool refused = base < 0 || base + n_new > cap;  // the whole append of this sequence is refused
+  if (refused && blockIdx.x == 0 && threadIdx.x == 0) set_dev_error(CSA2_ERR_BOUNDS);
+  if (e < n_new && !refused) quant_append_entry(lat, ikey, T, ratio, w0l, w1l, w0i, w1i, lat_codes, lat_scales,
+                                                idx_codes, idx_scales, cap, b, base, e, lane);
+  // a single block per sequence advances len itself (every thread has read it)
+  if (gridDim.x == 1) {
+    __syncthreads();
+    if (threadIdx.x == 0 && !refused) len[b] = (int32_t)(base + n_new);
+  }
 }
 
 // Advance len[b] by n_new after an append (refused appends leave len unchanged).
