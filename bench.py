@@ -233,23 +233,18 @@ def run_ours(args, rank, world, local):
     warm_graphs = max(1, -(-args.warmup // STEPS_PER_GRAPH))
     total_appends = (warm_graphs + n_graphs + 4) * STEPS_PER_GRAPH + args.e2e_steps + 16
     wl = CF.DecodeWorkload(c, extra=total_appends)
-    cache, layer = wl.cache, wl.layers[0]
+    cache = wl.cache
     tok_lat, tok_key = WL.new_token(c["seed"], 0, B, device="cuda")
-    q, q_idx, w_idx = layer.q, layer.q_idx, layer.w_idx
-    scores = torch.empty(B, cache.cap, dtype=torch.float32, device="cuda")
-    sel = torch.empty(B, CF.TOPK, dtype=torch.int32, device="cuda")
-    out = torch.empty(B, H, 512, dtype=torch.float32, device="cuda")
-    attn_ws = torch.empty(K.attn_workspace_size(B, H, CF.TOPK, 0), dtype=torch.uint8, device="cuda")
 
     def step(ev=None):
+        """One decode step: append this step's token to every sequence, then the Full
+        layer (indexer scan with its fused Top-512, gather + attention)."""
         K.kv_quant_append(tok_lat, tok_key, 1, cache)
         if ev is not None:
-            ev[0].record()
-        K.indexer_score(q_idx, w_idx, cache.idx_codes, cache.idx_scales, cache.len, scores=scores)
+            K.set_scan_events(ev[0], ev[1])
+        wl.step()
         if ev is not None:
-            ev[1].record()
-        K.topk_select(scores, CF.TOPK, n=cache.len, out=sel)
-        K.sparse_latent_attn(q, cache, sel, out=out, ws=attn_ws)
+            K.set_scan_events(None, None)
 
     # eager warm-up (sets kernel attributes before any capture), then graphs
     for _ in range(3):
@@ -257,6 +252,10 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
           for _ in range(K_steps)]
+    for a, b2 in ev:  # the hook takes raw event handles: create them on the device first
+        a.record()
+        b2.record()
+    torch.cuda.synchronize()
     graphs = []
     l0 = K.launch_count()
     for gi in range(n_graphs + warm_graphs):
@@ -310,7 +309,8 @@ def run_ours(args, rank, world, local):
         "data": "synthetic",
         "config": {"workload": c["name"], "sequences": B, "entries": N0, "heads": H, "indexer_heads": 4,
                    "topk": CF.TOPK, "q_dtype": "bf16", "latents": "fp32 N(0,1) x LogNormal(0,1) per channel",
-                   "step": "append 1 token/seq + indexer scan + Top-512 + sparse attention",
+                   "step": "kv_quant_append of 1 token/seq + csa2_decode_step (indexer scan with fused Top-512, "
+                           "gather + sparse attention)",
                    "l2": "inputs larger than L2 (1.5 GB cache)", "parallelism": f"replicas x{world}",
                    "cuda_graphs": f"{STEPS_PER_GRAPH} steps per graph"},
         "step_algorithmic_bytes": step_bytes,

@@ -180,3 +180,11 @@ def sync_status(stream=None) -> int:
 
 def launch_count() -> int:
     return A.lib().csa2_launch_count()
+
+
+def set_scan_events(before=None, after=None) -> None:
+    """Measurement hook: record the torch.cuda.Events ``before``/``after`` around every
+    indexer-scan launch made by later calls from this thread (None, None: off). The
+    events must already exist on the device (record them once first)."""
+    A.lib().csa2_set_scan_events(None if before is None else before.cuda_event,
+                                 None if after is None else after.cuda_event)

@@ -55,6 +55,7 @@ _PROTOS = {
     "csa2_sync_status": (C.c_int, [C.c_void_p]),
     "csa2_status_str": (C.c_char_p, [C.c_int]),
     "csa2_launch_count": (C.c_uint64, []),
+    "csa2_set_scan_events": (None, [C.c_void_p, C.c_void_p]),
 }
 
 

@@ -114,6 +114,12 @@ __device__ __forceinline__ uint32_t float_order_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Selection key of slot i with score s: (order(s) << 32) | (2^32-1 - i). Keys are
+// distinct, and a larger key is a higher score, then a lower slot.
+__device__ __forceinline__ unsigned long long topk_key(float s, uint32_t slot) {
+  return ((unsigned long long)float_order_key(s) << 32) | (unsigned long long)(0xFFFFFFFFu - slot);
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint32_t smem_u32addr(const void* p) { return smem_u32(p); }

@@ -82,10 +82,6 @@ __host__ __device__ constexpr size_t topk_smem_bytes(int k) {
   return sizeof(TopkCtl) + 8u * ((size_t)topk_cap(k) + topk_local_cap(k));
 }
 
-__device__ __forceinline__ unsigned long long topk_key(float s, uint32_t slot) {
-  return ((unsigned long long)float_order_key(s) << 32) | (unsigned long long)(0xFFFFFFFFu - slot);
-}
-
 // Exclusive scan over the block of one value per thread; *total gets the sum.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, TopkCtl& sh, uint32_t* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -425,6 +421,42 @@ __device__ void topk_whole_row(const RowSrc& rsrc, uint32_t n, int k, int32_t* o
     written += tot;
   }
   for (uint32_t j = written + tid; j < (uint32_t)k; j += kTopkThreads) orow[j] = -1;
+}
+
+// One block, one row of n scores (every slot valid): tau from up to 4096 evenly
+// spaced samples (about T keys expected >= tau), the keys >= tau filtered into
+// buf (cap keys), the exact K among them and the sorted output; the whole-row
+// select when the sample misses (fewer than min(k, n) or more than cap passed).
+__device__ void topk_row(const float* row, uint32_t n, int k, unsigned long long T, unsigned long long* buf,
+                         uint32_t cap, int32_t* orow, TopkCtl& sh) {
+  const int tid = threadIdx.x;
+  const RowSrc rsrc{row, nullptr};
+  const uint32_t S = n < 4096u ? n : 4096u;
+  unsigned long long tau = 1ull;
+  if ((unsigned long long)n > T) {
+    for (uint32_t s = tid; s < S; s += kTopkThreads) {
+      const uint32_t i = S == n ? s : (uint32_t)(((unsigned long long)s * n) / S);
+      buf[s] = rsrc(i);
+    }
+    __syncthreads();
+    unsigned long long r = (T * S + n - 1) / n;
+    r = r < 1 ? 1 : (r > S ? S : r);
+    tau = block_select(BufSrc{buf}, S, (uint32_t)r, sh, 2);
+  }
+  if (tid == 0) sh.lcount = 0;
+  __syncthreads();
+  const bool vec = ((uintptr_t)row & 15u) == 0;
+  topk_filter(row, nullptr, 0, n, vec, (uint32_t)(tau >> 32), (uint32_t)tau, buf, &sh.lcount, cap);
+  __syncthreads();
+  const uint32_t c = sh.lcount;
+  const uint32_t need = n < (uint32_t)k ? n : (uint32_t)k;
+  __syncthreads();
+  if (c <= cap && c >= need) {
+    const unsigned long long K = c > (uint32_t)k ? block_select(BufSrc{buf}, c, (uint32_t)k, sh) : 0ull;
+    topk_emit_sorted(buf, c, K, k, nullptr, orow, sh);
+    return;
+  }
+  topk_whole_row(rsrc, n, k, orow, sh);
 }
 
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)

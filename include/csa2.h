@@ -222,6 +222,19 @@ CSA2_API const char* csa2_status_str(csa2_status status);
 /* Number of kernels this library launched since load (host counter). */
 CSA2_API uint64_t csa2_launch_count(void);
 
+/*
+ * csa2_set_scan_events -- measurement hook for the dominant kernel.
+ *
+ * Not an operation of the method: lets a benchmark time the indexer scan inside
+ * indexer_score and csa2_decode_step. ``before``/``after`` are cudaEvent_t
+ * handles (NULL, NULL turns the hook off) that later calls made from this host
+ * thread record on their stream right before and right after each streaming
+ * indexer-scan launch (as external event nodes while the stream is being
+ * captured into a CUDA graph). The caller owns the events and keeps them alive
+ * while the hook is set.
+ */
+CSA2_API void csa2_set_scan_events(void* before, void* after);
+
 #ifdef __cplusplus
 }
 #endif

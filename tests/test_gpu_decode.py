@@ -123,3 +123,33 @@ def test_config3_full_size_sampled():
 @pytest.mark.slow
 def test_config4_full_size_sampled():
     _run(4, sample=[0, 63])
+
+
+def test_fused_select_misleading_sample_falls_back_exactly():
+    """The decode step's fused Top-k takes its threshold from 1,024 evenly spaced
+    entries. Giving exactly those entries the largest keys puts the threshold
+    inside that group, so too few candidates pass the scan's filter and both
+    fall-back stages run; the selection must still equal the exact Top-512."""
+    import torch
+    import fp4_compressed_kv_append_b300 as K
+    from fp4_compressed_kv_append_b300 import workloads as WL
+    B, N, k = 2, 131072, 512
+    cap = N + 128
+    cache = K.Cache(B, cap)
+    lc, ls, ic, isc = WL.random_cache_bytes(7, B, cap, device="cuda", scale_lo=118, scale_hi=122)
+    sampled = (torch.arange(1024, device="cuda") * N) // 1024
+    isc[:, sampled] = 134                                  # 2^7 larger key scales at the sampled positions
+    for name, t in zip(("lat_codes", "lat_scales", "idx_codes", "idx_scales"), (lc, ls, ic, isc)):
+        getattr(cache, name).copy_(t)
+    cache.len.fill_(N)
+    q, q_idx, w = WL.queries(7, 0, B, 64, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(B, 64, 512, dtype=torch.float32, device="cuda")
+    idx = torch.empty(B, k, dtype=torch.int32, device="cuda")
+    K.DecodeStep([K.Layer(K.FULL, q, out, cache=cache, q_idx=q_idx, w_idx=w, idx_out=idx)], k)()
+    torch.cuda.synchronize()
+    assert K.sync_status() == 0
+    for b in range(B):
+        keys = O.entry_keys(np_(cache.idx_codes[b, :N]), np_(cache.idx_scales[b, :N]))
+        s = O.indexer_scores(np_(q_idx[b]).astype(np.float64), np_(w[b]), keys)
+        ref = O.topk_positions(s, k)
+        Hh.assert_topk_match(np_(idx[b]), ref, s, where=f"seq {b}")
