@@ -309,7 +309,7 @@ def run_ours(args, rank, world, local):
         "data": "synthetic",
         "config": {"workload": c["name"], "sequences": B, "entries": N0, "heads": H, "indexer_heads": 4,
                    "topk": CF.TOPK, "q_dtype": "bf16", "latents": "fp32 N(0,1) x LogNormal(0,1) per channel",
-                   "step": "kv_quant_append of 1 token/seq + csa2_decode_step (indexer scan with fused Top-512, "
+                   "step": "kv_quant_append of 1 token/seq + csa2_decode_step (indexer scan, cluster Top-512, "
                            "gather + sparse attention)",
                    "l2": "inputs larger than L2 (1.5 GB cache)", "parallelism": f"replicas x{world}",
                    "cuda_graphs": f"{STEPS_PER_GRAPH} steps per graph"},

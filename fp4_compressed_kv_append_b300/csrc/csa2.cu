@@ -10,7 +10,6 @@
 #include "quant_append.cuh"
 #include "indexer_scan.cuh"
 #include "topk.cuh"
-#include "fused_select.cuh"
 #include "attention.cuh"
 
 namespace csa2 {
@@ -148,13 +147,29 @@ void launch_scan_tma(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s)
   k_indexer_scan_tma<NPART><<<grid, kTmaThreads, kTmaSmem, s>>>(m, a);
 }
 
-// Scores of every entry (cand == NULL) or of a candidate list; with f != NULL
-// (k <= kFusedMaxK, every entry) also the per-row thresholds and the candidate
-// lists of the fused Top-k, finished by launch_select_candidates. Returns false
-// when the fused form could not be used (nothing launched for it).
-bool launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
+void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
                  int64_t cap, const int32_t* len, const int32_t* cand, int P, float* scores, int batch,
-                 cudaStream_t s, const FusedSelectArgs* f = nullptr, int k = 0) {
+                 cudaStream_t s) {
+  g_launches += 1;
+  CUtensorMap m;
+  if (!cand && cap % kTmaRows == 0 && make_codes_map(&m, codes, (int64_t)batch * cap)) {
+    TmaScanArgs t;
+    t.q_idx = q_idx;
+    t.q_dtype = (int)dt;
+    t.w = w;
+    t.codes = codes;
+    t.scales = scales;
+    t.cap = cap;
+    t.len = len;
+    t.scores = scores;
+    t.tiles_per_seq = cap / kTmaRows;
+    t.total_tiles = t.tiles_per_seq * batch;
+    record_hook_event(g_scan_ev_before, s);
+    if (dt == CSA2_F32) launch_scan_tma<2>(m, t, s);
+    else launch_scan_tma<1>(m, t, s);
+    record_hook_event(g_scan_ev_after, s);
+    return;
+  }
   ScanArgs a;
   a.q_idx = q_idx;
   a.q_dtype = (int)dt;
@@ -169,55 +184,8 @@ bool launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
   a.stride = cand ? P : cap;
   a.tiles_per_seq = (a.stride + kScanTile - 1) / kScanTile;
   a.total_tiles = a.tiles_per_seq * batch;
-  CUtensorMap m;
-  if (!cand && cap % kTmaRows == 0 && make_codes_map(&m, codes, (int64_t)batch * cap)) {
-    TmaScanArgs t;
-    t.q_idx = q_idx;
-    t.q_dtype = (int)dt;
-    t.w = w;
-    t.codes = codes;
-    t.scales = scales;
-    t.cap = cap;
-    t.len = len;
-    t.scores = scores;
-    t.tiles_per_seq = cap / kTmaRows;
-    t.total_tiles = t.tiles_per_seq * batch;
-    t.tau = nullptr;
-    t.cand_count = nullptr;
-    t.cand_keys = nullptr;
-    t.cand_cap = kFusedCap;
-    if (f) {
-      t.tau = f->tau;
-      t.cand_count = f->cand_count;
-      t.cand_keys = f->cand_keys;
-      if (dt == CSA2_F32) k_row_threshold<2><<<batch, kTopkThreads, 0, s>>>(a, k, *f);
-      else k_row_threshold<1><<<batch, kTopkThreads, 0, s>>>(a, k, *f);
-      g_launches += 1;
-    }
-    record_hook_event(g_scan_ev_before, s);
-    if (dt == CSA2_F32) launch_scan_tma<2>(m, t, s);
-    else launch_scan_tma<1>(m, t, s);
-    record_hook_event(g_scan_ev_after, s);
-    g_launches += 1;
-    return true;
-  }
-  if (f) return false;
   if (dt == CSA2_F32) launch_scan_gather<2>(a, s);
   else launch_scan_gather<1>(a, s);
-  g_launches += 1;
-  return true;
-}
-
-void launch_select_candidates(const float* scores, int64_t cap, const int32_t* len, int k,
-                              const FusedSelectArgs& f, int32_t* out, int batch, cudaStream_t s) {
-  static bool attr_set = false;
-  const int smem = (int)(sizeof(TopkCtl) + 8u * kFusedCap);
-  if (!attr_set) {
-    cudaFuncSetAttribute(k_select_candidates, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attr_set = true;
-  }
-  k_select_candidates<<<batch, kTopkThreads, smem, s>>>(scores, cap, len, k, f, out);
-  g_launches += 1;
 }
 
 void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,
@@ -325,7 +293,7 @@ size_t csa2_topk_workspace_size(int32_t batch, int64_t stride, int32_t k) {
 
 namespace {
 struct StepLayout {
-  size_t scores, pool, pscores, sel, tau, ccount, ckeys, attn, total;
+  size_t scores, pool, pscores, sel, attn, total;
 };
 
 StepLayout step_layout(int32_t batch, int64_t max_entries, int32_t H, int32_t k, int32_t pool, int32_t W) {
@@ -339,14 +307,6 @@ StepLayout step_layout(int32_t batch, int64_t max_entries, int32_t H, int32_t k,
   off += round_up((size_t)batch * (size_t)pool * sizeof(float), 256);
   L.sel = off;
   off += round_up((size_t)batch * (size_t)k * sizeof(int32_t), 256);
-  // fused Top-k (k <= kFusedMaxK): per-row threshold, count and candidate list
-  const size_t fb = k <= kFusedMaxK ? (size_t)batch : 0;
-  L.tau = off;
-  off += round_up(fb * sizeof(unsigned long long), 256);
-  L.ccount = off;
-  off += round_up(fb * sizeof(uint32_t), 256);
-  L.ckeys = off;
-  off += round_up(fb * kFusedCap * sizeof(unsigned long long), 256);
   L.attn = off;
   off += attn_ws_bytes(batch, H, k, W);
   L.total = off;
@@ -398,23 +358,14 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
   float* pscores = reinterpret_cast<float*>(base + SL.pscores);
   int32_t* sel = reinterpret_cast<int32_t*>(base + SL.sel);
   void* attn_ws = base + SL.attn;
-  FusedSelectArgs fsa;
-  fsa.tau = reinterpret_cast<unsigned long long*>(base + SL.tau);
-  fsa.cand_count = reinterpret_cast<uint32_t*>(base + SL.ccount);
-  fsa.cand_keys = reinterpret_cast<unsigned long long*>(base + SL.ckeys);
-
   cudaStream_t s = (cudaStream_t)stream;
-  // Top-k of every entry of a cache: fused with the scan when k allows it
+  // Top-k of every entry of a cache: scores, then the cluster select
   auto scan_and_select = [&](const void* qi, const float* wi, const uint8_t* kc, const uint8_t* ksc,
                              const csa2_cache_view* c, int32_t* out_idx) {
-    if (k <= kFusedMaxK &&
-        launch_scan(qi, dtype, wi, kc, ksc, c->cap, c->len, nullptr, 0, scores, batch, s, &fsa, k)) {
-      launch_select_candidates(scores, c->cap, c->len, k, fsa, out_idx, batch, s);
-      return;
-    }
     launch_scan(qi, dtype, wi, kc, ksc, c->cap, c->len, nullptr, 0, scores, batch, s);
     launch_topk(scores, c->len, c->cap, k, nullptr, out_idx, batch, s);
   };
+
   const csa2_cache_view* main = nullptr;
   const int32_t* last = nullptr;
   int pool = 0;

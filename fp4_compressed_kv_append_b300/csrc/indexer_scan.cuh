@@ -321,13 +321,6 @@ struct TmaScanArgs {
   float* scores;
   int64_t tiles_per_seq;  // cap / 128
   int64_t total_tiles;
-  // optional candidate filter (all NULL: off): every entry of row b whose key
-  // (topk_key of its score and position) is >= tau[b] is appended to
-  // cand_keys[b][0 .. cand_cap) at cand_count[b] (the count goes on past cand_cap)
-  const unsigned long long* tau;
-  uint32_t* cand_count;
-  unsigned long long* cand_keys;
-  int cand_cap;
 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -470,8 +463,6 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
     uint32_t bf[2][4][NPART][2];
     float wsel0 = 0.f, wsel1 = 0.f;
     int setup_b = -1;
-    float tau_f = 0.f;
-    uint32_t tau_e = 0;
     uint32_t it = 0;
     int b = b0;
     int64_t e0 = e00;
@@ -481,12 +472,6 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
         if (b != setup_b) {
           scan_setup<NPART>(b, sa, lane, g, t4, bf, wsel0, wsel1);
           setup_b = b;
-          if (a.tau) {  // key >= tau  <=>  score > tau_f, or score == tau_f and position <= tau_e
-            const unsigned long long tb = __ldg(a.tau + b);
-            const uint32_t th = (uint32_t)(tb >> 32);
-            tau_f = __uint_as_float((th & 0x80000000u) ? (th & 0x7FFFFFFFu) : ~th);
-            tau_e = 0xFFFFFFFFu - (uint32_t)tb;
-          }
         }
         const uint32_t s = it % kTmaStages, ph = (it / kTmaStages) & 1u;
         if (!mbar_wait_bounded(bar_full + 8 * s, ph, abort)) break;
@@ -505,19 +490,9 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
         ++it;
         float s_lo, s_hi;
         scan_m16<NPART>(wl, wh, sl, sh, bf, wsel0, wsel1, s_lo, s_hi);
-        const int64_t e = e0 + (t4 ? rh : rl);
-        const float sc = t4 ? s_hi : s_lo;
-        if (t4 < 2 && e < n_b) a.scores[(size_t)b * a.cap + e] = sc;
-        if (a.tau) {  // lanes t4 = 0 and 1 hold the 16 scores of this m16 tile
-          const bool pass = t4 < 2 && e < n_b && (sc > tau_f || (sc == tau_f && (uint32_t)e <= tau_e));
-          const unsigned mask = __ballot_sync(0xffffffffu, pass);
-          if (mask) {
-            uint32_t base = 0;
-            if (lane == 0) base = atomicAdd(a.cand_count + b, (uint32_t)__popc(mask));
-            base = __shfl_sync(0xffffffffu, base, 0) + __popc(mask & ((1u << lane) - 1u));
-            if (pass && base < (uint32_t)a.cand_cap)
-              a.cand_keys[(size_t)b * a.cand_cap + base] = topk_key(sc, (uint32_t)e);
-          }
+        if (t4 < 2) {
+          const int64_t e = e0 + (t4 ? rh : rl);
+          if (e < n_b) a.scores[(size_t)b * a.cap + e] = t4 ? s_hi : s_lo;
         }
       }
       e0 += kTmaRows;
@@ -528,63 +503,6 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
       }
     }
   }
-}
-
-// ---------------------------------------------------------------- row thresholds
-// For the candidate filter of the streaming scan: one block per row scores
-// kThreshSamples evenly spaced entries (the same tensor-core m16 tiles, rows
-// gathered) and keeps their keys; tau[b] is a lower bound of the sample key of
-// rank r = ceil(T * samples / len[b]), so that about T keys of the row are
-// expected >= tau[b] (tau = 1, every entry, when len[b] <= T). cand_count[b] is
-// reset to 0 for the scan that follows.
-constexpr int kThreshSamples = 1024;
-
-template <int NPART, class SelectFn>
-__device__ void scan_threshold_row(const ScanArgs& a, int b, unsigned long long T, unsigned long long* keys,
-                                   SelectFn select, unsigned long long* tau_out) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, t4 = lane & 3;
-  const int64_t n_b = min((int64_t)__ldg(a.len + b), a.cap);
-  const uint32_t S = n_b < kThreshSamples ? (uint32_t)n_b : (uint32_t)kThreshSamples;
-  if ((uint64_t)n_b <= T) {
-    if (tid == 0) *tau_out = 1ull;
-    return;
-  }
-  uint32_t bf[2][4][NPART][2];
-  float wsel0, wsel1;
-  scan_setup<NPART>(b, a, lane, g, t4, bf, wsel0, wsel1);
-  const uint64_t pol = l2_evict_first_policy();
-  // warp w scores samples 32 * (w + 8 j) .. + 31 as one 32-entry tile
-  for (uint32_t s0 = 32 * w; s0 < S; s0 += 32 * (kScanThreads / 32)) {
-    uint32_t wr[4][4], sr[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint32_t s = s0 + g + 8 * r;
-      const bool ok = s < S;
-      const int64_t pos = ok ? (int64_t)(((uint64_t)s * (uint64_t)n_b) / S) : 0;
-      const size_t row = (size_t)b * a.cap + pos;
-      const uint8_t* cp = a.codes + row * 64 + 4 * t4;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) wr[r][j] = ok ? ldg_stream_u32(cp + 16 * j, pol) : 0u;
-      sr[r] = ok ? ldg_stream_u32(a.scales + row * 4, pol) >> (8 * (t4 >> 1)) : 0u;
-    }
-#pragma unroll
-    for (int st = 0; st < 2; ++st) {
-      float s_lo, s_hi;
-      scan_m16<NPART>(wr[2 * st], wr[2 * st + 1], sr[2 * st], sr[2 * st + 1], bf, wsel0, wsel1, s_lo, s_hi);
-      if (t4 < 2) {
-        const uint32_t s = s0 + g + 16 * st + 8 * t4;
-        if (s < S) {
-          const uint32_t pos = (uint32_t)(((uint64_t)s * (uint64_t)n_b) / S);
-          keys[s] = topk_key(t4 ? s_hi : s_lo, pos);
-        }
-      }
-    }
-  }
-  __syncthreads();
-  unsigned long long r = (T * S + (uint64_t)n_b - 1) / (uint64_t)n_b;
-  r = r < 1 ? 1 : (r > S ? S : r);
-  const unsigned long long tau = select(keys, S, (uint32_t)r);
-  if (tid == 0) *tau_out = tau;
 }
 
 }  // namespace csa2

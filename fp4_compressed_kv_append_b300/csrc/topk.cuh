@@ -11,15 +11,16 @@
 //
 // One cluster of kTopkCluster blocks per row; block r owns slice r of the row.
 // Small k (<= 1024):
-//  A. block r samples its slice and takes tau_r, a lower bound of the sample key
-//     of rank ceil(T_r * samples / valid_r), T_r = T / blocks (T = (k + CAP)/2
-//     keys wanted per row);
+//  A. block r samples its slice and takes tau_r, the smallest key sharing its
+//     12-bit prefix (sign, exponent, 3 mantissa bits) with the sample key of rank
+//     ceil(T_r * samples / valid_r), T_r = 3k / blocks;
 //  B. block r appends its keys >= tau_r to a local buffer, reserves room in block
 //     0's buffer (one remote atomic) and copies them there; after this cluster
 //     barrier only block 0 goes on;
 //  C. block 0: if the candidates number at least k, K is the k-th largest; they
 //     hold every key >= K when K >= max_r tau_r, and the k keys >= K are
-//     compacted and bitonic-sorted by slot. With fewer than k candidates, all of
+//     written in slot order through a slot bitmap (rows of up to kBitmapSlots;
+//     longer rows: compacted and bitonic-sorted). With fewer than k candidates, all of
 //     them when every tau_r was 1 (fewer than k valid slots). Otherwise (an
 //     unlucky sample) block 0 selects over the whole row: slower, same result.
 // Large k (the hierarchical pool): every block sends samples to block 0, which
@@ -55,12 +56,15 @@ constexpr int kSelBins = 1 << kSelBits;
 // Block 0's candidate buffer (keys), a block's local buffer (keys; none for large
 // k) and the row's sample count, by k. Shared memory per block: sizeof(TopkCtl)
 // + 8 (cap + local).
-__host__ __device__ constexpr uint32_t topk_cap(int k) { return k <= 1024 ? 4096u : 24576u; }
+__host__ __device__ constexpr uint32_t topk_cap(int k) { return k <= 1024 ? 6144u : 24576u; }
 __host__ __device__ constexpr uint32_t topk_local_cap(int k) { return k <= 1024 ? 2048u : 0u; }
 __host__ __device__ constexpr uint32_t topk_samples(int k) { return k <= 1024 ? 2048u : 16384u; }
 
+constexpr int kPrefixBins = 4096;        // 12-bit key prefixes (sign, exponent, 3 mantissa bits)
+constexpr uint32_t kBitmapSlots = 131072; // ordered output through a slot bitmap up to this row length
+
 struct TopkCtl {
-  uint32_t hist[kSelBins];
+  uint32_t hist[kPrefixBins];
   unsigned long long small[32];
   uint32_t warp_u32[32];
   unsigned long long warp_a[32], warp_b[32];
@@ -79,7 +83,7 @@ struct TopkCtl {
 };
 
 __host__ __device__ constexpr size_t topk_smem_bytes(int k) {
-  return sizeof(TopkCtl) + 8u * ((size_t)topk_cap(k) + topk_local_cap(k));
+  return sizeof(TopkCtl) + 8u * ((size_t)topk_cap(k) + topk_local_cap(k)) + (k <= 1024 ? kBitmapSlots / 8 : 0);
 }
 
 // Exclusive scan over the block of one value per thread; *total gets the sum.
@@ -360,6 +364,75 @@ __device__ __forceinline__ void topk_filter(const float* row, const int32_t* cro
   }
 }
 
+// Lower bound of the rank-th largest of the nonzero keys src(i), i < n: the
+// smallest key whose 12-bit prefix is that of the rank-th largest (one histogram
+// of prefixes, one scan from the top). 1 <= rank <= number of nonzero keys.
+template <class Src>
+__device__ unsigned long long block_prefix_bound(const Src& src, uint32_t n, uint32_t rank, TopkCtl& sh) {
+  const int tid = threadIdx.x;
+  for (int j = tid; j < kPrefixBins; j += kTopkThreads) sh.hist[j] = 0;
+  __syncthreads();
+  for (uint32_t i = tid; i < n; i += kTopkThreads) {
+    const unsigned long long x = src(i);
+    if (x) atomicAdd(&sh.hist[(uint32_t)(x >> 52)], 1u);
+  }
+  __syncthreads();
+  constexpr int P = kPrefixBins / kTopkThreads;
+  const int btop = kPrefixBins - 1 - P * tid;
+  uint32_t own = 0;
+#pragma unroll
+  for (int j = 0; j < P; ++j) own += sh.hist[btop - j];
+  uint32_t tot;
+  const uint32_t above = block_excl_scan(own, sh, &tot);
+  if (above < rank && above + own >= rank) {
+    uint32_t acc = above;
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      const uint32_t h = sh.hist[btop - j];
+      if (acc < rank && acc + h >= rank) sh.bc_u32[0] = (uint32_t)(btop - j);
+      acc += h;
+    }
+  }
+  __syncthreads();
+  const unsigned long long r = (unsigned long long)sh.bc_u32[0] << 52;
+  __syncthreads();
+  return r < 1ull ? 1ull : r;
+}
+
+// Block 0, rows of at most kBitmapSlots slots: mark the slots of the keys >= K
+// among buf[0..c) in a bitmap, then write them in slot order (one block scan over
+// the words), padded with -1 up to k.
+__device__ void topk_emit_bitmap(const unsigned long long* buf, uint32_t c, unsigned long long K, uint32_t n,
+                                 int k, const int32_t* crow, int32_t* orow, uint32_t* bits, TopkCtl& sh) {
+  const int tid = threadIdx.x;
+  const uint32_t nw = (n + 31) / 32;
+  for (uint32_t j = tid; j < nw; j += kTopkThreads) bits[j] = 0;
+  __syncthreads();
+  for (uint32_t j = tid; j < c; j += kTopkThreads) {
+    const unsigned long long x = buf[j];
+    if (x >= K) {
+      const uint32_t slot = 0xFFFFFFFFu - (uint32_t)x;
+      atomicOr(bits + (slot >> 5), 1u << (slot & 31));
+    }
+  }
+  __syncthreads();
+  const uint32_t wpt = (nw + kTopkThreads - 1) / kTopkThreads;
+  const uint32_t w0 = tid * wpt < nw ? tid * wpt : nw, w1 = w0 + wpt < nw ? w0 + wpt : nw;
+  uint32_t mine = 0;
+  for (uint32_t w = w0; w < w1; ++w) mine += __popc(bits[w]);
+  uint32_t total;
+  uint32_t at = block_excl_scan(mine, sh, &total);
+  for (uint32_t w = w0; w < w1 && at < (uint32_t)k; ++w) {
+    uint32_t m = bits[w];
+    while (m && at < (uint32_t)k) {
+      const uint32_t slot = 32 * w + (__ffs(m) - 1);
+      m &= m - 1;
+      orow[at++] = crow ? __ldg(crow + slot) : (int32_t)slot;
+    }
+  }
+  for (uint32_t j = total + tid; j < (uint32_t)k; j += kTopkThreads) orow[j] = -1;
+}
+
 // Block 0: write the slots of the keys >= K among buf[0..c) (all when K is 0) in
 // ascending slot order as positions, padded with -1 up to k (in-place ordered
 // compaction, then a bitonic sort).
@@ -423,42 +496,6 @@ __device__ void topk_whole_row(const RowSrc& rsrc, uint32_t n, int k, int32_t* o
   for (uint32_t j = written + tid; j < (uint32_t)k; j += kTopkThreads) orow[j] = -1;
 }
 
-// One block, one row of n scores (every slot valid): tau from up to 4096 evenly
-// spaced samples (about T keys expected >= tau), the keys >= tau filtered into
-// buf (cap keys), the exact K among them and the sorted output; the whole-row
-// select when the sample misses (fewer than min(k, n) or more than cap passed).
-__device__ void topk_row(const float* row, uint32_t n, int k, unsigned long long T, unsigned long long* buf,
-                         uint32_t cap, int32_t* orow, TopkCtl& sh) {
-  const int tid = threadIdx.x;
-  const RowSrc rsrc{row, nullptr};
-  const uint32_t S = n < 4096u ? n : 4096u;
-  unsigned long long tau = 1ull;
-  if ((unsigned long long)n > T) {
-    for (uint32_t s = tid; s < S; s += kTopkThreads) {
-      const uint32_t i = S == n ? s : (uint32_t)(((unsigned long long)s * n) / S);
-      buf[s] = rsrc(i);
-    }
-    __syncthreads();
-    unsigned long long r = (T * S + n - 1) / n;
-    r = r < 1 ? 1 : (r > S ? S : r);
-    tau = block_select(BufSrc{buf}, S, (uint32_t)r, sh, 2);
-  }
-  if (tid == 0) sh.lcount = 0;
-  __syncthreads();
-  const bool vec = ((uintptr_t)row & 15u) == 0;
-  topk_filter(row, nullptr, 0, n, vec, (uint32_t)(tau >> 32), (uint32_t)tau, buf, &sh.lcount, cap);
-  __syncthreads();
-  const uint32_t c = sh.lcount;
-  const uint32_t need = n < (uint32_t)k ? n : (uint32_t)k;
-  __syncthreads();
-  if (c <= cap && c >= need) {
-    const unsigned long long K = c > (uint32_t)k ? block_select(BufSrc{buf}, c, (uint32_t)k, sh) : 0ull;
-    topk_emit_sorted(buf, c, K, k, nullptr, orow, sh);
-    return;
-  }
-  topk_whole_row(rsrc, n, k, orow, sh);
-}
-
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
 k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ nvec,
        const int32_t* __restrict__ cand, int k, int32_t* __restrict__ out) {
@@ -469,6 +506,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
   unsigned long long* gbuf = reinterpret_cast<unsigned long long*>(smem_raw + sizeof(TopkCtl));
   const uint32_t CAP = topk_cap(k), LCAP = topk_local_cap(k);
   unsigned long long* lbuf = gbuf + CAP;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(lbuf + LCAP);  // small k, block 0: slot bitmap
   const uint32_t rank = cluster.block_rank();
   TopkCtl& sh0 = *cluster.map_shared_rank(&sh, 0);
   unsigned long long* gbuf0 = cluster.map_shared_rank(gbuf, 0);
@@ -503,12 +541,12 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
 
   if (LCAP > 0) {
     // ================= small k: local thresholds, block 0 finishes alone
-    // A. tau_r: about T/clusters keys of this slice are expected >= tau_r
-    const uint32_t S0 = topk_samples(k);
+    // A. tau_r: about T/clusters keys of this slice are expected >= tau_r (T = 3k)
+    const uint32_t S0 = topk_samples(k);  // a power of two
     const uint32_t S = slen < S0 ? slen : S0;
     uint32_t sv = 0;
     for (uint32_t s = tid; s < S; s += kTopkThreads) {
-      const uint32_t i = lo_slot + (S == slen ? s : (uint32_t)(((unsigned long long)s * slen) / S));
+      const uint32_t i = lo_slot + (S == slen ? s : (uint32_t)(((unsigned long long)s * slen) >> (__ffs(S0) - 1)));
       const unsigned long long key = rsrc(i);
       lbuf[s] = key;
       sv += key != 0ull;
@@ -517,11 +555,11 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
     unsigned long long tau = 1ull;
     uint32_t mr = slen;  // valid slots of the slice, estimated from the sample for candidate lists
     if (crow && S > 0) mr = (uint32_t)(((unsigned long long)sv * slen + S - 1) / S);
-    const unsigned long long Tr = (T + kTopkCluster - 1) / kTopkCluster;
+    const unsigned long long Tr = (3ull * (unsigned long long)k + kTopkCluster - 1) / kTopkCluster;
     if (sv > 0 && mr > Tr) {
       unsigned long long r = (Tr * sv + mr - 1) / mr;
       r = r < 1 ? 1 : (r > sv ? sv : r);
-      tau = block_select(BufSrc{lbuf}, S, (uint32_t)r, sh, 2);
+      tau = block_prefix_bound(BufSrc{lbuf}, S, (uint32_t)r, sh);
     }
     // B. keys >= tau_r into the local buffer, then block 0's buffer
     topk_filter(row, crow, lo_slot, hi_slot, vec, (uint32_t)(tau >> 32), (uint32_t)tau, lbuf, &sh.lcount, LCAP);
@@ -550,11 +588,13 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
       if (c >= (uint32_t)k) {
         const unsigned long long K = block_select(BufSrc{gbuf}, c, (uint32_t)k, sh);
         if (K >= taumax) {
-          topk_emit_sorted(gbuf, c, K, k, crow, orow, sh);
+          if (n <= kBitmapSlots) topk_emit_bitmap(gbuf, c, K, n, k, crow, orow, bits, sh);
+          else topk_emit_sorted(gbuf, c, K, k, crow, orow, sh);
           return;
         }
       } else if (taumax == 1ull) {  // every valid slot passed: fewer than k valid
-        topk_emit_sorted(gbuf, c, 0ull, k, crow, orow, sh);
+        if (n <= kBitmapSlots) topk_emit_bitmap(gbuf, c, 1ull, n, k, crow, orow, bits, sh);
+        else topk_emit_sorted(gbuf, c, 0ull, k, crow, orow, sh);
         return;
       }
     }

@@ -125,11 +125,11 @@ def test_config4_full_size_sampled():
     _run(4, sample=[0, 63])
 
 
-def test_fused_select_misleading_sample_falls_back_exactly():
-    """The decode step's fused Top-k takes its threshold from 1,024 evenly spaced
-    entries. Giving exactly those entries the largest keys puts the threshold
-    inside that group, so too few candidates pass the scan's filter and both
-    fall-back stages run; the selection must still equal the exact Top-512."""
+def test_decode_step_misleading_sample_falls_back_exactly():
+    """Top-k takes its candidate threshold from evenly spaced samples of each slice.
+    Giving every 128th entry (a subset of the samples) much larger keys puts the
+    thresholds inside that group, so too few candidates pass and the exact
+    whole-row selection runs; the result must still equal the exact Top-512."""
     import torch
     import fp4_compressed_kv_append_b300 as K
     from fp4_compressed_kv_append_b300 import workloads as WL
