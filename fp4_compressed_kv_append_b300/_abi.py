@@ -15,6 +15,7 @@ OK, ERR_ARG, ERR_ALIGN, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS, ERR_
 F32, BF16 = 0, 1
 FULL, REINDEX, REUSE = 0, 1, 2
 LATENT_DIM, INDEXER_DIM, INDEXER_HEADS, MAX_TOPK, MAX_WINDOW = 512, 128, 4, 16384, 1024
+STATIC_WS_BYTES = 24 << 20  # CSA2_STATIC_WS_BYTES
 
 
 class CacheView(C.Structure):
@@ -49,6 +50,8 @@ _PROTOS = {
                                      C.c_void_p]),
     "csa2_decode_step": (C.c_int, [C.POINTER(LayerDesc), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int,
                                    C.c_void_p, C.c_size_t, C.c_void_p]),
+    "csa2_decode_step_static": (C.c_int, [C.POINTER(LayerDesc), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int,
+                                          C.c_void_p]),
     "csa2_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "csa2_topk_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32]),
     "csa2_attn_workspace_size": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),

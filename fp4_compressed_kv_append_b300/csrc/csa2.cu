@@ -3,6 +3,7 @@
 // caller's stream. The library allocates no device memory.
 #include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include <cuda.h>
 
@@ -436,6 +437,35 @@ uint64_t csa2_launch_count(void) { return g_launches.load(); }
 void csa2_set_scan_events(void* before, void* after) {
   g_scan_ev_before = static_cast<cudaEvent_t>(before);
   g_scan_ev_after = static_cast<cudaEvent_t>(after);
+}
+
+// ---------------------------------------------------------------- allocation-free decode step
+// Scratch of csa2_decode_step_static: one file-scope device array, present on every
+// device that loads this library until the process exits. Host code only ever uses
+// its per-device address from cudaGetSymbolAddress (the symbol itself is a host-side
+// stand-in there).
+static __device__ __align__(256) unsigned char g_static_ws[CSA2_STATIC_WS_BYTES];
+
+namespace {
+std::mutex g_static_ws_mutex;
+void* g_static_ws_ptr[64] = {nullptr};
+}  // namespace
+
+csa2_status csa2_decode_step_static(const csa2_layer_desc* layers, int32_t n_layers, int32_t batch, int32_t H,
+                                    int32_t k, csa2_dtype dtype, csa2_stream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+    if (!g_static_ws_ptr[dev]) {  // first call on this device: look the array up (device is current)
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return CSA2_ERR_CUDA;
+      g_static_ws_ptr[dev] = p;
+    }
+    ws = g_static_ws_ptr[dev];
+  }
+  return csa2_decode_step(layers, n_layers, batch, H, k, dtype, ws, (size_t)CSA2_STATIC_WS_BYTES, stream);
 }
 
 }  // extern "C"

@@ -72,6 +72,9 @@ enum {
   CSA2_MAX_WINDOW = 1024  /* largest sliding window */
 };
 
+/* Size of the device scratch built into the library for csa2_decode_step_static. */
+#define CSA2_STATIC_WS_BYTES (24u << 20) /* 24 MiB */
+
 /* One layer's global cache (host struct holding device pointers). */
 typedef struct {
   uint8_t* lat_codes;  /* [batch][cap][256] */
@@ -203,6 +206,33 @@ typedef struct {
 CSA2_API csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, int32_t batch,
                              int32_t H, int32_t k, csa2_dtype dtype, void* ws, size_t ws_bytes,
                              csa2_stream_t stream);
+
+/*
+ * csa2_decode_step_static -- csa2_decode_step without a caller-provided workspace.
+ *
+ * The pages have no counterpart to this call: it is a convenience of the library.
+ * Some callers cannot allocate device memory at the point where they run a decode
+ * step: a host program without a device allocator of its own, a plug-in that
+ * must not touch the allocator of the framework that hosts it, or a serving loop
+ * that forbids allocation after start-up. This entry point runs the same step
+ * (same arguments and results as csa2_decode_step) with its scratch in an array
+ * of CSA2_STATIC_WS_BYTES (24 MiB) compiled into the library; it allocates and
+ * frees nothing. The caller still owns every input and output.
+ *   - A step that needs more than CSA2_STATIC_WS_BYTES of scratch
+ *     (csa2_workspace_size() > CSA2_STATIC_WS_BYTES; for instance more than
+ *     about six million cached entries over the batch) is rejected with
+ *     CSA2_ERR_WORKSPACE and launches nothing.
+ *   - Every device that loads the library keeps the array until the process
+ *     exits. The first call on a device (with that device current) looks the
+ *     array up with cudaGetSymbolAddress; make that first call before any stream
+ *     capture on the device.
+ *   - All calls share the one array: calls that may overlap on the GPU (other
+ *     streams, other host threads) race on it and must be serialised by the
+ *     caller. Nothing in it needs to start at zero; it keeps the last call's
+ *     contents.
+ */
+CSA2_API csa2_status csa2_decode_step_static(const csa2_layer_desc* layers, int32_t n_layers, int32_t batch,
+                                             int32_t H, int32_t k, csa2_dtype dtype, csa2_stream_t stream);
 
 /* Scratch bytes of csa2_decode_step for these sizes (max_entries = cap). */
 CSA2_API size_t csa2_workspace_size(int32_t batch, int64_t max_entries, int32_t H, int32_t k, int32_t pool,
