@@ -10,6 +10,7 @@
 #include "common.cuh"
 #include "quant_append.cuh"
 #include "indexer_scan.cuh"
+#include "indexer_scan_tc.cuh"
 #include "topk.cuh"
 #include "attention.cuh"
 
@@ -148,6 +149,35 @@ void launch_scan_tma(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s)
   k_indexer_scan_tma<NPART><<<grid, kTmaThreads, kTmaSmem, s>>>(m, a);
 }
 
+template <int NPART>
+void launch_scan_tc(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s) {
+  using S = TcShape<NPART>;
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    cudaFuncSetAttribute(k_indexer_scan_tc<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::Smem);
+    // two blocks per SM: their 256-column tensor-memory allocations fill the SM's 512
+    // columns, and registers (96 x 320 per block) and shared memory allow two
+    int dev = 0, smem_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    per_sm = smem_sm >= 2 * (S::Smem + 1024) ? 2 : 1;
+  }
+  const int64_t full = (int64_t)sm_count() * per_sm;
+  const int grid = (int)(a.total_tiles < full ? a.total_tiles : full);
+  k_indexer_scan_tc<NPART><<<grid, kTcThreads, S::Smem, s>>>(m, a);
+}
+
+// Which streaming scan runs: the mma.sync form unless CSA2_SCAN_KERNEL=tc asks for
+// the tcgen05 form (read once).
+bool scan_uses_tcgen05() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("CSA2_SCAN_KERNEL");
+    v = (e && strcmp(e, "tc") == 0) ? 1 : 0;
+  }
+  return v == 1;
+}
+
 void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
                  int64_t cap, const int32_t* len, const int32_t* cand, int P, float* scores, int batch,
                  cudaStream_t s) {
@@ -166,8 +196,13 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
     t.tiles_per_seq = cap / kTmaRows;
     t.total_tiles = t.tiles_per_seq * batch;
     record_hook_event(g_scan_ev_before, s);
-    if (dt == CSA2_F32) launch_scan_tma<2>(m, t, s);
-    else launch_scan_tma<1>(m, t, s);
+    if (scan_uses_tcgen05()) {
+      if (dt == CSA2_F32) launch_scan_tc<2>(m, t, s);
+      else launch_scan_tc<1>(m, t, s);
+    } else {
+      if (dt == CSA2_F32) launch_scan_tma<2>(m, t, s);
+      else launch_scan_tma<1>(m, t, s);
+    }
     record_hook_event(g_scan_ev_after, s);
     return;
   }

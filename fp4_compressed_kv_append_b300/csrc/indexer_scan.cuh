@@ -14,11 +14,13 @@
 //    the packed codes with cvt.rn.f16x2.e2m1x2 -- exact in fp16.
 //  * Operand B (16 channels x 8 columns): the queries, scaled per head by a power
 //    of two 2^s_h so that fp16 keeps every bit of a bf16 query (fp32 queries are
-//    split into fp16 hi + lo parts, a second n-tile). Column n = 4*jj + h holds
+//    split into fp16 hi + lo parts, a second n-tile). Column n = 2*h + jj holds
 //    head h restricted to block jj of a pair of 32-channel blocks (zero
 //    elsewhere), so one MMA keeps two E8M0 blocks apart and every column is used.
-//  * Epilogue: per block, multiply by its exact power-of-two scale, add the four
-//    blocks, undo 2^s_h inside the head weight, ReLU, weighted head sum.
+//  * Epilogue: lane t4 of a quad holds head t4's four block dots of its two rows;
+//    it multiplies each by the block's exact power-of-two scale (E8M0 -> bf16 by
+//    cvt.rn.bf16x2.ue8m0x2), adds them, applies the ReLU and the head weight (with
+//    2^-s_h folded in), and two quad shuffles sum the heads.
 //
 // Lane (g = lane/4, t4 = lane%4) of a warp loads, for entries g + 8r (r = 0..3),
 // the 32-bit word t4 of each 16-byte block of codes -- so a k-step's channels
@@ -81,17 +83,10 @@ __device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// 2^(e-127) for the E8M0 byte e = bits [7:0] of w (e < 255): the byte moved to the
-// float exponent field; byte 0 becomes the subnormal 2^-127 (bit pattern 0x00400000,
-// the unsigned maximum of the two, since every e >= 1 gives at least 0x00800000).
-__device__ __forceinline__ float e8m0_low_byte(uint32_t w) {
-  return __uint_as_float(max((w << 23) & 0x7F800000u, 0x00400000u));
-}
-
 // ------------------------------------------------------------------ tile registers
 struct ScanTile {
   uint32_t w[4][4];  // [row r = entry g + 8r][block j]: code word t4 of block j
-  uint32_t s[4];     // the entry's four E8M0 bytes, shifted right by 8*(t4>>1)
+  uint32_t s[4];     // the entry's four E8M0 bytes
   int b;             // sequence
   int64_t e0;        // first entry (or candidate slot) of the tile
   uint32_t flags;    // bit r: slot in range; bit 4+r: entry valid
@@ -137,7 +132,7 @@ __device__ __forceinline__ void scan_load_tile(ScanTile& T, int64_t t, const Sca
       const uint8_t* cp = a.codes + row * 64 + 4 * t4;
 #pragma unroll
       for (int j = 0; j < 4; ++j) T.w[r][j] = ldg_stream_u32(cp + 16 * j, pol);
-      T.s[r] = ldg_stream_u32(a.scales + row * 4, pol) >> (8 * (t4 >> 1));
+      T.s[r] = ldg_stream_u32(a.scales + row * 4, pol);
     } else {
 #pragma unroll
       for (int j = 0; j < 4; ++j) T.w[r][j] = 0;
@@ -149,7 +144,7 @@ __device__ __forceinline__ void scan_load_tile(ScanTile& T, int64_t t, const Sca
 // Query fragments of sequence b. NPART = 1 (bf16 queries) or 2 (fp32: hi, lo).
 template <int NPART>
 __device__ __forceinline__ void scan_setup(int b, const ScanArgs& a, int lane, int g, int t4,
-                                           uint32_t (&bf)[2][4][NPART][2], float& wsel0, float& wsel1) {
+                                           uint32_t (&bf)[2][4][NPART][2], float& wsel) {
   const size_t qb = (size_t)b * CSA2_INDEXER_HEADS * CSA2_INDEXER_DIM;
   float f[CSA2_INDEXER_HEADS], winv[CSA2_INDEXER_HEADS];
 #pragma unroll
@@ -166,11 +161,11 @@ __device__ __forceinline__ void scan_setup(int b, const ScanArgs& a, int lane, i
     f[h] = __uint_as_float((uint32_t)(127 + s) << 23);     // 2^s, exact
     winv[h] = __ldg(a.w + (size_t)b * CSA2_INDEXER_HEADS + h) * __uint_as_float((uint32_t)(127 - s) << 23);
   }
-  const int h0 = 2 * (t4 & 1);
-  wsel0 = (h0 == 0) ? winv[0] : winv[2];
-  wsel1 = (h0 == 0) ? winv[1] : winv[3];
-  // column n = g: jj = g >> 2 (block of the pair), head hh = g & 3
-  const int jj = g >> 2, hh = g & 3;
+  wsel = winv[0];
+#pragma unroll
+  for (int h = 1; h < CSA2_INDEXER_HEADS; ++h) wsel = t4 == h ? winv[h] : wsel;
+  // column n = g: head hh = g >> 1, block jj = g & 1 of the pair
+  const int jj = g & 1, hh = g >> 1;
   float fh = f[0];
 #pragma unroll
   for (int h = 1; h < CSA2_INDEXER_HEADS; ++h) fh = hh == h ? f[h] : fh;
@@ -195,12 +190,25 @@ __device__ __forceinline__ void scan_setup(int b, const ScanArgs& a, int lane, i
   }
 }
 
+// The four E8M0 bytes of w as floats (2^(e-127), exact; 0xFF gives NaN).
+__device__ __forceinline__ void e8m0x4_decode(uint32_t w, float (&sc)[4]) {
+  uint32_t s01, s23;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n"
+      " cvt.rn.bf16x2.ue8m0x2 %0, lo;\n cvt.rn.bf16x2.ue8m0x2 %1, hi;\n}\n"
+      : "=r"(s01), "=r"(s23)
+      : "r"(w));
+  sc[0] = __uint_as_float(s01 << 16);
+  sc[1] = __uint_as_float(s01 & 0xFFFF0000u);
+  sc[2] = __uint_as_float(s23 << 16);
+  sc[3] = __uint_as_float(s23 & 0xFFFF0000u);
+}
+
 // One m16 row tile: rows g (words wl, scale word sl) and g+8 (wh, sh) of a
-// 16-entry group. Returns the scores of both rows (in every lane of the quad).
+// 16-entry group. Returns the score of row g in lanes with even t4 and of row g+8
+// in lanes with odd t4.
 template <int NPART>
-__device__ __forceinline__ void scan_m16(const uint32_t (&wl)[4], const uint32_t (&wh)[4], uint32_t sl, uint32_t sh,
-                                         const uint32_t (&bf)[2][4][NPART][2], float wsel0, float wsel1,
-                                         float& score_lo, float& score_hi) {
+__device__ __forceinline__ float scan_m16(const uint32_t (&wl)[4], const uint32_t (&wh)[4], uint32_t sl, uint32_t sh,
+                                          const uint32_t (&bf)[2][4][NPART][2], float wsel, int t4) {
   float acc[2][NPART][4];
 #pragma unroll
   for (int p = 0; p < 2; ++p)
@@ -219,35 +227,29 @@ __device__ __forceinline__ void scan_m16(const uint32_t (&wl)[4], const uint32_t
       for (int nt = 0; nt < NPART; ++nt)
         mma_16816(acc[p][nt], lo0[kq], hi0[kq], lo1[kq], hi1[kq], bf[p][kq][nt][0], bf[p][kq][nt][1]);
   }
-  // this lane's columns 2t4, 2t4+1 = block 2p + (t4>>1), heads 2(t4&1) + {0,1};
-  // sl/sh hold the entry's scale bytes shifted right by 8*(t4>>1)
-  float v[2][2];
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const uint32_t sw = rr ? sh : sl;
-    const float sc0 = e8m0_low_byte(sw), sc1 = e8m0_low_byte(sw >> 16);
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float c0 = acc[0][0][2 * rr + e], c1 = acc[1][0][2 * rr + e];
-      if constexpr (NPART == 2) {
-        c0 += acc[0][1][2 * rr + e];
-        c1 += acc[1][1][2 * rr + e];
-      }
-      v[rr][e] = fmaf(c1, sc1, c0 * sc0);
-    }
-  }
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) v[rr][e] += __shfl_xor_sync(0xffffffffu, v[rr][e], 2);
+  // acc[p][.][2 rr + jj]: row g + 8 rr, column 2 t4 + jj = head t4, block 2p + jj
   float part[2];
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
-    part[rr] = fmaf(wsel1, fmaxf(v[rr][1], 0.f), wsel0 * fmaxf(v[rr][0], 0.f));
-    part[rr] += __shfl_xor_sync(0xffffffffu, part[rr], 1);
+    float sc[4];
+    e8m0x4_decode(rr ? sh : sl, sc);
+    float d[4];
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        d[2 * p + jj] = acc[p][0][2 * rr + jj];
+        if constexpr (NPART == 2) d[2 * p + jj] += acc[p][1][2 * rr + jj];
+      }
+    const float v = fmaf(d[3], sc[3], fmaf(d[2], sc[2], fmaf(d[1], sc[1], d[0] * sc[0])));
+    part[rr] = wsel * fmaxf(v, 0.f);
   }
-  score_lo = part[0];
-  score_hi = part[1];
+  // heads: lanes t4 and t4^1 trade the row the other one keeps, then t4 ^ 2
+  const bool odd = (t4 & 1) != 0;
+  float keep = odd ? part[1] : part[0];
+  keep += __shfl_xor_sync(0xffffffffu, odd ? part[0] : part[1], 1);
+  keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+  return keep;
 }
 
 // ---------------------------------------------------------------- gather form
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan_gather(const S
   const uint64_t pol = l2_evict_first_policy();
 
   uint32_t bf[2][4][NPART][2];
-  float wsel0 = 0.f, wsel1 = 0.f;
+  float wsel = 0.f;
   int setup_b = -1;
 
   ScanTile cur, nxt;
@@ -272,19 +274,18 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan_gather(const S
   for (int64_t t = t_begin; t < t_end; ++t) {
     if (t + 1 < t_end) scan_load_tile(nxt, t + 1, a, g, t4, pol);
     if (cur.b != setup_b) {
-      scan_setup<NPART>(cur.b, a, lane, g, t4, bf, wsel0, wsel1);
+      scan_setup<NPART>(cur.b, a, lane, g, t4, bf, wsel);
       setup_b = cur.b;
     }
 #pragma unroll
     for (int st = 0; st < 2; ++st) {  // rows (2st, 2st+1) = entries g + 16st (+8)
       const int rl = 2 * st, rh = 2 * st + 1;
-      float s_lo, s_hi;
-      scan_m16<NPART>(cur.w[rl], cur.w[rh], cur.s[rl], cur.s[rh], bf, wsel0, wsel1, s_lo, s_hi);
+      const float sc = scan_m16<NPART>(cur.w[rl], cur.w[rh], cur.s[rl], cur.s[rh], bf, wsel, t4);
       if (t4 < 2) {  // lane t4 == 0 stores row rl, lane t4 == 1 row rh
         const int r = t4 ? rh : rl;
         if ((cur.flags >> r) & 1u) {
           const int64_t e = cur.e0 + g + 8 * r;
-          a.scores[(size_t)cur.b * a.stride + e] = ((cur.flags >> (4 + r)) & 1u) ? (t4 ? s_hi : s_lo) : -INFINITY;
+          a.scores[(size_t)cur.b * a.stride + e] = ((cur.flags >> (4 + r)) & 1u) ? sc : -INFINITY;
         }
       }
     }
@@ -461,7 +462,7 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
     sa.q_dtype = a.q_dtype;
     sa.w = a.w;
     uint32_t bf[2][4][NPART][2];
-    float wsel0 = 0.f, wsel1 = 0.f;
+    float wsel = 0.f;
     int setup_b = -1;
     uint32_t it = 0;
     int b = b0;
@@ -470,7 +471,7 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
     for (int64_t t = t_begin; t < t_end; ++t) {
       if (e0 < n_b) {
         if (b != setup_b) {
-          scan_setup<NPART>(b, sa, lane, g, t4, bf, wsel0, wsel1);
+          scan_setup<NPART>(b, sa, lane, g, t4, bf, wsel);
           setup_b = b;
         }
         const uint32_t s = it % kTmaStages, ph = (it / kTmaStages) & 1u;
@@ -483,16 +484,15 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
           wl[j] = *reinterpret_cast<const uint32_t*>(st + 64 * rl + off);
           wh[j] = *reinterpret_cast<const uint32_t*>(st + 64 * rh + off);
         }
-        const uint32_t sl = *reinterpret_cast<const uint32_t*>(st + kTmaRows * 64 + 4 * rl) >> (8 * (t4 >> 1));
-        const uint32_t sh = *reinterpret_cast<const uint32_t*>(st + kTmaRows * 64 + 4 * rh) >> (8 * (t4 >> 1));
+        const uint32_t sl = *reinterpret_cast<const uint32_t*>(st + kTmaRows * 64 + 4 * rl);
+        const uint32_t sh = *reinterpret_cast<const uint32_t*>(st + kTmaRows * 64 + 4 * rh);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         ++it;
-        float s_lo, s_hi;
-        scan_m16<NPART>(wl, wh, sl, sh, bf, wsel0, wsel1, s_lo, s_hi);
+        const float sc = scan_m16<NPART>(wl, wh, sl, sh, bf, wsel, t4);
         if (t4 < 2) {
           const int64_t e = e0 + (t4 ? rh : rl);
-          if (e < n_b) a.scores[(size_t)b * a.cap + e] = t4 ? s_hi : s_lo;
+          if (e < n_b) a.scores[(size_t)b * a.cap + e] = sc;
         }
       }
       e0 += kTmaRows;

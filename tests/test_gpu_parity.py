@@ -120,6 +120,29 @@ def test_indexer_scores_within_fp32_bound(dtype):
         assert np.all(err <= tol), (b, float((err / tol).max()))
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_indexer_scores_long_rows_ragged_lengths(dtype):
+    # many 128-entry tiles per block, sequences that end inside a tile, an empty
+    # sequence and a one-entry sequence; keys are uniformly random bytes
+    B, cap = 5, 65536
+    lens = [cap, 0, 1, 40001, cap - 1]
+    _, _, ic, isc = WL.random_cache_bytes(11, B, cap, device="cuda", scale_lo=118, scale_hi=136)
+    ln = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    _, q_idx, w = WL.queries(2, "scan", B, 16, dtype=dtype, device="cuda")
+    scores = K.indexer_score(q_idx, w, ic, isc, ln)
+    torch.cuda.synchronize()
+    assert K.sync_status() == 0
+    ic_h, isc_h = np_(ic), np_(isc)
+    for b, n in enumerate(lens):
+        if n == 0:
+            continue
+        keys = O.entry_keys(ic_h[b, :n], isc_h[b, :n])
+        ref = O.indexer_scores(np_(q_idx[b]).astype(np.float64), np_(w[b]), keys)
+        tol = Hh.score_tolerance(np_(q_idx[b]), np_(w[b]), keys)
+        err = np.abs(np_(scores[b, :n]).astype(np.float64) - ref)
+        assert np.all(err <= tol), (b, float((err / tol).max()))
+
+
 def test_indexer_scores_on_candidates():
     B, N, P = 2, 1500, 700
     cache, host = _small_cache(B, N)
