@@ -193,7 +193,8 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
     t.cap = cap;
     t.len = len;
     t.scores = scores;
-    t.tiles_per_seq = cap / kTmaRows;
+    const int64_t tile_rows = scan_uses_tcgen05() ? kTmaRows : kTmaStageRows;
+    t.tiles_per_seq = (cap + tile_rows - 1) / tile_rows;
     t.total_tiles = t.tiles_per_seq * batch;
     record_hook_event(g_scan_ev_before, s);
     if (scan_uses_tcgen05()) {

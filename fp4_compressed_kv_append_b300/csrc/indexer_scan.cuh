@@ -306,9 +306,10 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan_gather(const S
 // chunk, rows g and g+8) free of bank conflicts.
 constexpr int kTmaConsumers = 8;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
-constexpr int kTmaRows = 128;
-constexpr int kTmaStages = 8;
-constexpr int kTmaStageBytes = 9216;  // 8192 code bytes (1024-aligned) + 512 scale bytes
+constexpr int kTmaRows = 128;        // rows of one TMA box
+constexpr int kTmaStageRows = 256;   // rows of one stage: two boxes, 32 per consumer warp
+constexpr int kTmaStages = 4;
+constexpr int kTmaStageBytes = 17408;  // 16384 code bytes (1024-aligned) + 1024 scale bytes
 constexpr int kTmaSmem = kTmaStages * kTmaStageBytes + 2 * kTmaStages * 8 + 64 + 1024;
 
 struct TmaScanArgs {
@@ -320,7 +321,7 @@ struct TmaScanArgs {
   int64_t cap;
   const int32_t* len;
   float* scores;
-  int64_t tiles_per_seq;  // cap / 128
+  int64_t tiles_per_seq;  // ceil(cap / tile rows): 256-row stages (mma.sync form), 128 (tcgen05 form)
   int64_t total_tiles;
 };
 
@@ -417,7 +418,8 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
   const int64_t t_begin = (int64_t)blockIdx.x * a.total_tiles / gridDim.x;
   const int64_t t_end = (int64_t)(blockIdx.x + 1) * a.total_tiles / gridDim.x;
   int b0 = (int)(t_begin / a.tiles_per_seq);
-  int64_t e00 = (t_begin - (int64_t)b0 * a.tiles_per_seq) * kTmaRows;
+  int64_t e00 = (t_begin - (int64_t)b0 * a.tiles_per_seq) * kTmaStageRows;
+  const int64_t seq_rows = a.tiles_per_seq * kTmaStageRows;
 
   if (warp == kTmaConsumers) {
     // ---------------- producer (one lane)
@@ -434,13 +436,17 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
           if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort)) break;
           const uint32_t st = sbase + s * kTmaStageBytes;
           const int64_t row = (int64_t)b * a.cap + e0;
-          mbar_arrive_expect_tx(bar_full + 8 * s, kTmaRows * 64 + kTmaRows * 4);
+          // the last stage of a sequence holds one box when cap is an odd multiple of 128
+          const uint32_t rows = a.cap - e0 >= kTmaStageRows ? kTmaStageRows : kTmaRows;
+          mbar_arrive_expect_tx(bar_full + 8 * s, rows * 68);
           tma_load_rows(st, &tmap, 0, (int32_t)row, bar_full + 8 * s, pol);
-          bulk_load(st + kTmaRows * 64, a.scales + row * 4, kTmaRows * 4, bar_full + 8 * s, pol);
+          if (rows == kTmaStageRows)
+            tma_load_rows(st + kTmaRows * 64, &tmap, 0, (int32_t)(row + kTmaRows), bar_full + 8 * s, pol);
+          bulk_load(st + kTmaStageRows * 64, a.scales + row * 4, rows * 4, bar_full + 8 * s, pol);
           ++it;
         }
-        e0 += kTmaRows;
-        if (e0 >= a.tiles_per_seq * kTmaRows && t + 1 < t_end) {
+        e0 += kTmaStageRows;
+        if (e0 >= seq_rows && t + 1 < t_end) {
           e0 = 0;
           ++b;
           n_b = min((int64_t)__ldg(a.len + b), a.cap);
@@ -453,10 +459,11 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
       }
     }
   } else {
-    // ---------------- consumers: warp w owns rows 16w .. 16w+15 of every stage
+    // ---------------- consumers: warp w owns rows 32w .. 32w+31 of every stage
+    // (two m16 tiles: rows 32w + g + 8r, r = 0..3)
     const int g = lane >> 2, t4 = lane & 3;
-    const int rl = 16 * warp + g, rh = rl + 8;
-    const uint32_t swz = (uint32_t)((g >> 1) & 3);  // same for rl and rh
+    const int r0 = 32 * warp + g;
+    const uint32_t swz = (uint32_t)((g >> 1) & 3);  // the same for every row r0 + 8r
     ScanArgs sa;
     sa.q_idx = a.q_idx;
     sa.q_dtype = a.q_dtype;
@@ -477,26 +484,28 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
         const uint32_t s = it % kTmaStages, ph = (it / kTmaStages) & 1u;
         if (!mbar_wait_bounded(bar_full + 8 * s, ph, abort)) break;
         const unsigned char* st = smem + s * kTmaStageBytes;
-        uint32_t wl[4], wh[4];
+        uint32_t w[4][4], sw[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t off = 16u * ((uint32_t)j ^ swz) + 4u * t4;
-          wl[j] = *reinterpret_cast<const uint32_t*>(st + 64 * rl + off);
-          wh[j] = *reinterpret_cast<const uint32_t*>(st + 64 * rh + off);
+        for (int r = 0; r < 4; ++r) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            w[r][j] = *reinterpret_cast<const uint32_t*>(st + 64 * (r0 + 8 * r) + 16u * ((uint32_t)j ^ swz) + 4u * t4);
+          sw[r] = *reinterpret_cast<const uint32_t*>(st + kTmaStageRows * 64 + 4 * (r0 + 8 * r));
         }
-        const uint32_t sl = *reinterpret_cast<const uint32_t*>(st + kTmaRows * 64 + 4 * rl);
-        const uint32_t sh = *reinterpret_cast<const uint32_t*>(st + kTmaRows * 64 + 4 * rh);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         ++it;
-        const float sc = scan_m16<NPART>(wl, wh, sl, sh, bf, wsel, t4);
-        if (t4 < 2) {
-          const int64_t e = e0 + (t4 ? rh : rl);
-          if (e < n_b) a.scores[(size_t)b * a.cap + e] = sc;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {  // rows r0 + 16m (even t4 stores) and r0 + 16m + 8 (odd t4)
+          const float sc = scan_m16<NPART>(w[2 * m], w[2 * m + 1], sw[2 * m], sw[2 * m + 1], bf, wsel, t4);
+          if (t4 < 2) {
+            const int64_t e = e0 + r0 + 16 * m + 8 * t4;
+            if (e < n_b) a.scores[(size_t)b * a.cap + e] = sc;
+          }
         }
       }
-      e0 += kTmaRows;
-      if (e0 >= a.tiles_per_seq * kTmaRows && t + 1 < t_end) {
+      e0 += kTmaStageRows;
+      if (e0 >= seq_rows && t + 1 < t_end) {
         e0 = 0;
         ++b;
         n_b = min((int64_t)__ldg(a.len + b), a.cap);

@@ -105,10 +105,11 @@ def _small_cache(B, N, seed=1, cap=None):
     return cache, host
 
 
+@pytest.mark.parametrize("cap", [2560, 2688])  # an even and an odd multiple of 128 rows
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_indexer_scores_within_fp32_bound(dtype):
+def test_indexer_scores_within_fp32_bound(dtype, cap):
     B, N = 3, 2500
-    cache, host = _small_cache(B, N)
+    cache, host = _small_cache(B, N, cap=cap)
     _, q_idx, w = WL.queries(1, "scan", B, 16, dtype=dtype, device="cuda")
     scores = K.indexer_score(q_idx, w, cache.idx_codes, cache.idx_scales, cache.len)
     torch.cuda.synchronize()
