@@ -144,7 +144,7 @@ void launch_scan_tma(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s)
     cudaFuncSetAttribute(k_indexer_scan_tma<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem);
     attr_set = true;
   }
-  const int64_t full = (int64_t)sm_count() * 3;
+  const int64_t full = (int64_t)sm_count() * kTmaBlocksPerSM;
   const int grid = (int)(a.total_tiles < full ? a.total_tiles : full);
   k_indexer_scan_tma<NPART><<<grid, kTmaThreads, kTmaSmem, s>>>(m, a);
 }

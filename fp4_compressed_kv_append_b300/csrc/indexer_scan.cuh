@@ -294,23 +294,43 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan_gather(const S
 }
 
 // ---------------------------------------------------------------- streaming form
-// Scores every entry of every sequence. A producer warp streams 128-entry tiles
-// of codes (one TMA box of 128 rows x 64 bytes, 64-byte swizzle) and their E8M0
-// bytes (one 512-byte bulk copy) into a ring of shared-memory stages; eight
-// consumer warps take 16 rows each per stage. Three blocks share an SM. Full/empty mbarriers hand the
-// stages back and forth; every wait gives up after about a second, records
-// CSA2_ERR_TIMEOUT and stops the block.
+// Scores every entry of every sequence. A producer warp streams 512-entry stages
+// -- four TMA boxes of 128 rows x 64 bytes of codes (64-byte swizzle) and one bulk
+// copy of their E8M0 bytes -- into a ring of three shared-memory stages; eight
+// consumer warps take 64 rows (four m16 tiles) each per stage, so one wait and
+// one release cover four independent tiles. Two blocks share an SM (209 KB of
+// stages in flight per SM). Full/empty mbarriers hand the stages back and forth;
+// every wait gives up after about a second, records CSA2_ERR_TIMEOUT and stops
+// the block. (Measured on B300 at 32 x 131,072 entries: 16-row warp tiles and
+// 128-row stages ran at 3.8 TB/s, 32-row tiles at 4.6, 64-row tiles at 5.2.)
 //
 // With the 64-byte swizzle the 16-byte chunk j of row r sits at chunk
 // j ^ ((r >> 1) & 3), which makes the consumers' 32-bit loads (word t4 of each
-// chunk, rows g and g+8) free of bank conflicts.
-constexpr int kTmaConsumers = 8;
+// chunk, rows g + 8r) free of bank conflicts.
+#ifndef CSA2_SCAN_CONSUMERS
+#define CSA2_SCAN_CONSUMERS 8
+#endif
+constexpr int kTmaConsumers = CSA2_SCAN_CONSUMERS;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
-constexpr int kTmaRows = 128;        // rows of one TMA box
-constexpr int kTmaStageRows = 256;   // rows of one stage: two boxes, 32 per consumer warp
-constexpr int kTmaStages = 4;
-constexpr int kTmaStageBytes = 17408;  // 16384 code bytes (1024-aligned) + 1024 scale bytes
+#ifndef CSA2_SCAN_STAGE_ROWS
+#define CSA2_SCAN_STAGE_ROWS 512
+#endif
+#ifndef CSA2_SCAN_STAGES
+#define CSA2_SCAN_STAGES 3
+#endif
+#ifndef CSA2_SCAN_BLOCKS_PER_SM
+#define CSA2_SCAN_BLOCKS_PER_SM 2
+#endif
+constexpr int kTmaRows = 128;                           // rows of one TMA box
+constexpr int kTmaStageRows = CSA2_SCAN_STAGE_ROWS;     // rows of one stage (whole boxes)
+constexpr int kTmaWarpRows = kTmaStageRows / kTmaConsumers;
+constexpr int kTmaWarpM16 = kTmaWarpRows / 16;          // m16 tiles per consumer warp per stage
+constexpr int kTmaStages = CSA2_SCAN_STAGES;
+constexpr int kTmaBlocksPerSM = CSA2_SCAN_BLOCKS_PER_SM;
+constexpr int kTmaStageBytes = kTmaStageRows * 68;      // codes, then the E8M0 bytes
 constexpr int kTmaSmem = kTmaStages * kTmaStageBytes + 2 * kTmaStages * 8 + 64 + 1024;
+static_assert(kTmaStageRows % kTmaRows == 0 && kTmaWarpRows % 16 == 0, "stage shape");
+static_assert(kTmaStageBytes % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled boxes");
 
 struct TmaScanArgs {
   const void* q_idx;
@@ -394,7 +414,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 template <int NPART>
-__global__ void __launch_bounds__(kTmaThreads, 3)
+__global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSM)
 k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -436,12 +456,13 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
           if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort)) break;
           const uint32_t st = sbase + s * kTmaStageBytes;
           const int64_t row = (int64_t)b * a.cap + e0;
-          // the last stage of a sequence holds one box when cap is an odd multiple of 128
-          const uint32_t rows = a.cap - e0 >= kTmaStageRows ? kTmaStageRows : kTmaRows;
+          // the last stage of a sequence holds fewer boxes when cap is not a multiple of
+          // the stage rows (cap is a multiple of 128)
+          const int64_t left = a.cap - e0;
+          const uint32_t rows = left >= kTmaStageRows ? (uint32_t)kTmaStageRows : (uint32_t)left;
           mbar_arrive_expect_tx(bar_full + 8 * s, rows * 68);
-          tma_load_rows(st, &tmap, 0, (int32_t)row, bar_full + 8 * s, pol);
-          if (rows == kTmaStageRows)
-            tma_load_rows(st + kTmaRows * 64, &tmap, 0, (int32_t)(row + kTmaRows), bar_full + 8 * s, pol);
+          for (uint32_t q = 0; q < rows / kTmaRows; ++q)
+            tma_load_rows(st + q * kTmaRows * 64, &tmap, 0, (int32_t)(row + q * kTmaRows), bar_full + 8 * s, pol);
           bulk_load(st + kTmaStageRows * 64, a.scales + row * 4, rows * 4, bar_full + 8 * s, pol);
           ++it;
         }
@@ -459,10 +480,10 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
       }
     }
   } else {
-    // ---------------- consumers: warp w owns rows 32w .. 32w+31 of every stage
-    // (two m16 tiles: rows 32w + g + 8r, r = 0..3)
+    // ---------------- consumers: warp w owns rows kTmaWarpRows * w + g + 8r of every stage
+    // (kTmaWarpM16 m16 tiles)
     const int g = lane >> 2, t4 = lane & 3;
-    const int r0 = 32 * warp + g;
+    const int r0 = kTmaWarpRows * warp + g;
     const uint32_t swz = (uint32_t)((g >> 1) & 3);  // the same for every row r0 + 8r
     ScanArgs sa;
     sa.q_idx = a.q_idx;
@@ -484,9 +505,9 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
         const uint32_t s = it % kTmaStages, ph = (it / kTmaStages) & 1u;
         if (!mbar_wait_bounded(bar_full + 8 * s, ph, abort)) break;
         const unsigned char* st = smem + s * kTmaStageBytes;
-        uint32_t w[4][4], sw[4];
+        uint32_t w[2 * kTmaWarpM16][4], sw[2 * kTmaWarpM16];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < 2 * kTmaWarpM16; ++r) {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             w[r][j] = *reinterpret_cast<const uint32_t*>(st + 64 * (r0 + 8 * r) + 16u * ((uint32_t)j ^ swz) + 4u * t4);
@@ -496,7 +517,7 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         ++it;
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {  // rows r0 + 16m (even t4 stores) and r0 + 16m + 8 (odd t4)
+        for (int m = 0; m < kTmaWarpM16; ++m) {  // rows r0 + 16m (even t4 stores) and r0 + 16m + 8 (odd t4)
           const float sc = scan_m16<NPART>(w[2 * m], w[2 * m + 1], sw[2 * m], sw[2 * m + 1], bf, wsel, t4);
           if (t4 < 2) {
             const int64_t e = e0 + r0 + 16 * m + 8 * t4;
