@@ -229,11 +229,10 @@ void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, c
                  int32_t* out, int batch, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)topk_smem_bytes(CSA2_MAX_TOPK));
+    cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
     attr_set = true;
   }
-  k_topk<<<dim3(kTopkCluster, batch), kTopkThreads, topk_smem_bytes(k), s>>>(scores, stride, n, cand, k, out);
+  k_topk<<<dim3(kTopkCluster, batch), kTopkThreads, kTopkSmem, s>>>(scores, stride, n, cand, k, out);
   g_launches += 1;
 }
 

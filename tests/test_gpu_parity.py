@@ -250,7 +250,10 @@ def test_topk_unrepresentative_sample_takes_the_exact_fallback(sampled_high):
         assert np.array_equal(np_(out[b]), ref)
 
 
-@pytest.mark.parametrize("n,k", [(524288, 16384), (65536 + 77, 512), (20000, 1500)])
+# rows around the longest one kept in shared memory (8 x 18,432 = 147,456 slots), one
+# that is just too long for some blocks, and one of the decode cache's appended lengths
+@pytest.mark.parametrize("n,k", [(524288, 16384), (65536 + 77, 512), (20000, 1500), (147456, 512),
+                                 (147456 + 13, 512), (135200, 512), (300001, 2048)])
 def test_topk_large_rows(n, k):
     B = 2
     s = WL.scores(n + k, B, n, device="cpu", ties=100000)
