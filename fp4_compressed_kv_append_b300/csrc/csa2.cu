@@ -13,6 +13,7 @@
 #include "indexer_scan_tc.cuh"
 #include "topk.cuh"
 #include "attention.cuh"
+#include "attention_cl.cuh"
 
 namespace csa2 {
 namespace {
@@ -248,11 +249,54 @@ void launch_attn_t(const void* q, csa2_dtype dt, int H, float scale, const csa2_
       q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H, out);
 }
 
+// Key-split form: one cluster of ceil((k + W) / 128) blocks per (sequence, 64 heads).
+template <int NPART>
+void launch_attn_cl(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
+                    int k, const uint16_t* swa, int W, float* out, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(k_sparse_attn_cl<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAclSmem);
+    attr_set = true;
+  }
+  const int C = (k + W + kAclKeys - 1) / kAclKeys;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(C * (H / kAclHeads)), (unsigned)c.batch, 1);
+  cfg.blockDim = dim3(kAclThreads, 1, 1);
+  cfg.dynamicSmemBytes = kAclSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, k_sparse_attn_cl<NPART>, q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap,
+                     idx, k, swa, W, H, out);
+}
+
+// The key-split form covers 64-head groups and up to 1,024 keys per row; the
+// chunked form everything else. CSA2_ATTN_KERNEL=chunked forces the chunked form
+// (read once).
+bool attn_key_split(int H, int k, int W) {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("CSA2_ATTN_KERNEL");
+    v = (e && strcmp(e, "chunked") == 0) ? 0 : 1;
+  }
+  return v == 1 && H % kAclHeads == 0 && k + W >= 1 && k + W <= kAclKeys * kAclMaxBlocks;
+}
+
 void launch_attn(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
                  int k, const uint16_t* swa, int W, float* out, void* ws, cudaStream_t s) {
   (void)ws;
-  if (dt == CSA2_F32) launch_attn_t<2>(q, dt, H, scale, c, idx, k, swa, W, out, s);
-  else launch_attn_t<1>(q, dt, H, scale, c, idx, k, swa, W, out, s);
+  if (attn_key_split(H, k, W)) {
+    if (dt == CSA2_F32) launch_attn_cl<2>(q, dt, H, scale, c, idx, k, swa, W, out, s);
+    else launch_attn_cl<1>(q, dt, H, scale, c, idx, k, swa, W, out, s);
+  } else {
+    if (dt == CSA2_F32) launch_attn_t<2>(q, dt, H, scale, c, idx, k, swa, W, out, s);
+    else launch_attn_t<1>(q, dt, H, scale, c, idx, k, swa, W, out, s);
+  }
   g_launches += 1;
 }
 

@@ -199,7 +199,9 @@ def test_topk_with_candidates():
 @pytest.mark.parametrize("H,k,W,dtype", [(16, 512, 0, torch.float32), (64, 512, 0, torch.bfloat16),
                                          (32, 300, 0, torch.bfloat16), (64, 512, 128, torch.bfloat16),
                                          (64, 1, 77, torch.bfloat16), (64, 0, 128, torch.bfloat16),
-                                         (16, 129, 5, torch.float32), (64, 0, 0, torch.bfloat16)])
+                                         (16, 129, 5, torch.float32), (64, 0, 0, torch.bfloat16),
+                                         (64, 512, 0, torch.float32), (64, 700, 100, torch.bfloat16),
+                                         (64, 1024, 0, torch.bfloat16), (64, 1000, 24, torch.float32)])
 def test_attention_within_2e3(H, k, W, dtype):
     B, N = 2, 1200
     cache, host = _small_cache(B, N, seed=4)
