@@ -18,16 +18,23 @@ namespace csa2 {
 
 constexpr int kAppendWarps = 8;
 
+// Lane l's share of one packed entry.
+struct PackedLane {
+  uint32_t lo, hi;     // 16 latent codes
+  uint32_t s_code;     // their E4M3 scale
+  uint32_t kc;         // 4 indexer-key codes
+  uint32_t x_code;     // the E8M0 scale of the lane's 32-channel key block
+};
+
 // One entry: ratio-2 merge (optional), then both packings. Lane l of the warp.
+// Needs only the source token, not the cache position, so the loads do not wait
+// for the sequence length.
 template <typename Tin>
-__device__ __forceinline__ void quant_append_entry(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
-                                                   int ratio, const float* __restrict__ w0l,
-                                                   const float* __restrict__ w1l, const float* __restrict__ w0i,
-                                                   const float* __restrict__ w1i, uint8_t* __restrict__ lat_codes,
-                                                   uint8_t* __restrict__ lat_scales, uint8_t* __restrict__ idx_codes,
-                                                   uint8_t* __restrict__ idx_scales, int64_t cap, int b, int64_t base,
-                                                   int e, int lane) {
-  const int64_t slot = (size_t)b * cap + base + e;
+__device__ __forceinline__ PackedLane quant_entry(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
+                                                  int ratio, const float* __restrict__ w0l,
+                                                  const float* __restrict__ w1l, const float* __restrict__ w0i,
+                                                  const float* __restrict__ w1i, int b, int e, int lane) {
+  PackedLane P;
   const size_t tok = (size_t)b * T + (size_t)e * ratio;
 
   // ---- latent: one 16-channel block per lane
@@ -64,8 +71,9 @@ __device__ __forceinline__ void quant_append_entry(const Tin* __restrict__ lat, 
 #pragma unroll
     for (int i = 0; i < 8; ++i) hi |= e2m1_encode(__fdiv_rn(x[8 + i], s)) << (4 * i);
   }
-  *reinterpret_cast<uint2*>(lat_codes + slot * 256 + 8 * lane) = make_uint2(lo, hi);
-  lat_scales[slot * 32 + lane] = (uint8_t)s_code;
+  P.lo = lo;
+  P.hi = hi;
+  P.s_code = s_code;
 
   // ---- indexer key: four channels per lane, eight lanes per 32-channel block
   float z[4];
@@ -94,8 +102,19 @@ __device__ __forceinline__ void quant_append_entry(const Tin* __restrict__ lat, 
   uint32_t kc = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) kc |= e2m1_encode(z[i] * inv) << (4 * i);
-  *reinterpret_cast<uint16_t*>(idx_codes + slot * 64 + 2 * lane) = (uint16_t)kc;
-  if ((lane & 7) == 0) idx_scales[slot * 4 + (lane >> 3)] = (uint8_t)(X + 127);
+  P.kc = kc;
+  P.x_code = (uint32_t)(X + 127);
+  return P;
+}
+
+// Lane l's stores of an entry at cache slot `slot` (row index b * cap + position).
+__device__ __forceinline__ void store_entry(const PackedLane& P, uint8_t* __restrict__ lat_codes,
+                                            uint8_t* __restrict__ lat_scales, uint8_t* __restrict__ idx_codes,
+                                            uint8_t* __restrict__ idx_scales, int64_t slot, int lane) {
+  *reinterpret_cast<uint2*>(lat_codes + slot * 256 + 8 * lane) = make_uint2(P.lo, P.hi);
+  lat_scales[slot * 32 + lane] = (uint8_t)P.s_code;
+  *reinterpret_cast<uint16_t*>(idx_codes + slot * 64 + 2 * lane) = (uint16_t)P.kc;
+  if ((lane & 7) == 0) idx_scales[slot * 4 + (lane >> 3)] = (uint8_t)P.x_code;
 }
 
 template <typename Tin>
@@ -109,11 +128,13 @@ k_quant_append(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
   const int b = blockIdx.y;
-  const int64_t base = len[b];
+  const int64_t base = len[b];  // in flight while the entry is packed
+  PackedLane P{};
+  if (e < n_new) P = quant_entry(lat, ikey, T, ratio, w0l, w1l, w0i, w1i, b, e, lane);
   const bool refused = base < 0 || base + n_new > cap;  // the whole append of this sequence is refused
   if (refused && blockIdx.x == 0 && threadIdx.x == 0) set_dev_error(CSA2_ERR_BOUNDS);
-  if (e < n_new && !refused) quant_append_entry(lat, ikey, T, ratio, w0l, w1l, w0i, w1i, lat_codes, lat_scales,
-                                                idx_codes, idx_scales, cap, b, base, e, lane);
+  if (e < n_new && !refused)
+    store_entry(P, lat_codes, lat_scales, idx_codes, idx_scales, (int64_t)b * cap + base + e, lane);
   // a single block per sequence advances len itself (every thread has read it)
   if (gridDim.x == 1) {
     __syncthreads();
