@@ -34,6 +34,12 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 SCAN_BYTES_PER_ENTRY = 68     # indexer key: 64 B codes + 4 B E8M0 scales
+# DRAM read + write bytes per scanned entry of the streaming scan kernel, from one ncu
+# capture of it on 16 x 131,072 entries (146.86 MB / 2,097,152 entries): the keys read
+# once plus the score writes that reach DRAM during the launch. Traffic grows with the
+# entries scanned, so a launch's traffic is this figure times its entries. Valid for the
+# kernel as captured; it has to be measured again whenever the scan kernel changes.
+SCAN_TRAFFIC_PER_ENTRY = 70.03
 GATHER_BYTES_PER_ENTRY = 288  # latent: 256 B codes + 32 B E4M3 scales
 STEPS_PER_GRAPH = 16
 
@@ -316,7 +322,8 @@ def run_ours(args, rank, world, local):
         "step_algorithmic_bytes": step_bytes,
         "step_hbm_gbs": step_bytes / (ms / K_steps * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "indexer scan", "achieved": achieved, "peak": hbm_peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": SCAN_TRAFFIC_PER_ENTRY * scan_bytes_avg / SCAN_BYTES_PER_ENTRY,
                      "scan_ms": scan_avg_ms, "bytes_per_launch": scan_bytes_avg},
         "gpu_launches": int(round(launches_per_step * K_steps)),
         "clocks": sampler.summary(),
