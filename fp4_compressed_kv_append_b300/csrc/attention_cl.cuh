@@ -8,15 +8,19 @@
 // token", "Troisiemement" (E2M1 values with an E4M3 scale per 16 channels; a
 // 128-token sliding window kept outside the global cache).
 //
-// Per block (512 threads, 16 warps; shared memory: Q 64 KB + V 128 KB):
+// Per block (512 threads, 16 warps; shared memory: Q 64 KB + V 128 KB; 64 columns of
+// tensor memory):
 //  * thread t loads a quarter of key t/4 (64 code bytes, 8 E4M3 bytes) into
 //    registers at once, then the queries (per-head 2^s scaling as in the chunked
 //    form; fp32 queries as fp16 hi + lo, the lo part kept in registers) go to
 //    shared memory, then the keys are dequantised to fp16 (exact) into V;
-//  * S = Q V^T (mma.sync m16n8k16): warp (mt, kg) covers heads 16mt.. and keys
-//    32kg.. over all 512 dims;
-//  * softmax over the block's keys (base 2, max per head over the four key
-//    groups through shared memory), P rounded to fp16 and kept in the Q area;
+//  * S^T = V Q^T on the 5th-generation tensor cores: Q and V sit in shared memory
+//    in the tensor core's K-major 128-byte-swizzled layout, one thread issues 32
+//    tcgen05.mma (M = 128 keys, N = 64 heads, K = 16 each; fp32 queries: a second
+//    pass with the fp16 remainder) into tensor memory, and the warps read the
+//    logits back with tcgen05.ld;
+//  * softmax over the block's keys (base 2; eight lanes per head through a
+//    shared-memory copy of S), P rounded to fp16 and kept over the Q area;
 //  * O = P V: warp (mt, dq) owns heads 16mt.. and dims 128dq..;
 //  * the unnormalised O, max and sum of every block are staged in its shared
 //    memory; after a cluster barrier block r merges heads [64r/C, 64(r+1)/C) of
@@ -27,6 +31,7 @@
 #include <cooperative_groups.h>
 
 #include "attention.cuh"
+#include "indexer_scan_tc.cuh"
 
 namespace csa2 {
 
@@ -34,15 +39,22 @@ constexpr int kAclThreads = 512;
 constexpr int kAclKeys = 128;   // keys per block
 constexpr int kAclHeads = 64;   // heads per block
 constexpr int kAclMaxBlocks = 8;
-constexpr int kAclQ = 0;                                  // [64 heads][512] fp16 (swzv); later P [64][128]
-constexpr int kAclV = kAclQ + kAclHeads * 1024;           // [128 keys][512] fp16 (swzv)
+constexpr int kAclQ = 0;                                  // Q [64 heads][512] fp16, K-major 128-byte swizzle
+constexpr int kAclSSt = kAclQ;                            // after S: S [64 heads][128 keys] f32 over Q
+constexpr int kAclP = kAclQ + kAclHeads * kAclKeys * 4;   // after S: P [64 heads][128 keys] fp16 over Q
+constexpr int kAclV = kAclQ + kAclHeads * 1024;           // V [128 keys][512] fp16, K-major 128-byte swizzle
 constexpr int kAclRedM = kAclV + kAclKeys * 1024;         // [4 key groups][64] f32
 constexpr int kAclRedL = kAclRedM + 4 * kAclHeads * 4;    // [4][64] f32
 constexpr int kAclCoef = kAclRedL + 4 * kAclHeads * 4;    // [64] f32
 constexpr int kAclM = kAclCoef + kAclHeads * 4;           // [64] f32: this block's max per head
 constexpr int kAclL = kAclM + kAclHeads * 4;              // [64] f32: this block's sum per head
 constexpr int kAclKeyOk = kAclL + kAclHeads * 4;          // [128] i32
-constexpr int kAclSmem = kAclKeyOk + kAclKeys * 4;
+constexpr int kAclBar = kAclKeyOk + kAclKeys * 4;         // mbarrier (8 B), tensor-memory base (4 B), abort (4 B)
+constexpr int kAclSmem = kAclBar + 16 + 1024;             // + slack to align the base to 1024 bytes
+constexpr int kAclTmemCols = 64;                          // S^T: 128 lanes (keys) x 64 columns (heads)
+// instruction descriptor, kind::f16: D f32, A = B = f16, both K-major, M = 128, N = 64
+constexpr uint32_t kAclIDesc = (1u << 4) | ((uint32_t)(kAclHeads >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+static_assert(kAclP + kAclHeads * kAclKeys * 2 <= kAclV, "S and P fit over Q");
 constexpr int kAclOPitch = 520;                           // floats per staged O row (bank spread)
 constexpr int kAclO = 0;                                  // [64][520] f32 over Q and V, after O = P V
 static_assert(kAclO + kAclHeads * kAclOPitch * 4 <= kAclRedM, "staged O fits over Q and V");
@@ -51,13 +63,36 @@ static_assert((kAclMaxBlocks + 1) * kAclHeads * 4 <= kAclM - kAclRedM, "merge we
 // P [64 heads][128 keys] fp16: 16-byte chunk c of row h.
 __device__ __forceinline__ uint32_t acl_pidx(int h, int c) { return (uint32_t)(h * 256 + ((c ^ (h & 7)) << 4)); }
 
+// The tensor core's K-major, 128-byte-swizzled operand layout: 16-byte chunk c (dims
+// 8c .. 8c+7) of row r sits in the 64-dim block c/8, in row r of that block (128 B
+// per row, blocks of `rows` rows), at chunk (c mod 8) XOR (r mod 8). The same layout
+// serves the ldmatrix reads of O = P V (eight consecutive rows of one chunk column hit
+// eight bank groups).
+__device__ __forceinline__ uint32_t acl_kidx(int r, int c, int rows) {
+  return (uint32_t)((c >> 3) * (rows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ uint32_t acl_vidx(int key, int c) { return acl_kidx(key, c, kAclKeys); }
+__device__ __forceinline__ uint32_t acl_qidx(int h, int c) { return acl_kidx(h, c, kAclHeads); }
+
+// D[tmem] (+)= A[smem descriptor] x B[smem descriptor], kind::f16.
+__device__ __forceinline__ void tc_mma_f16_ss(uint32_t d_taddr, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_taddr),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 template <int NPART>
 __global__ void __launch_bounds__(kAclThreads, 1)
 k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uint8_t* __restrict__ lat_codes,
                  const uint8_t* __restrict__ lat_scales, const int32_t* __restrict__ len, int64_t cap,
                  const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int W, int H,
                  float* __restrict__ out) {
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
@@ -67,12 +102,19 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
   const int g = lane >> 2, t4 = lane & 3;
   unsigned char* qs = smem + kAclQ;
   unsigned char* vs = smem + kAclV;
-  float* red_m = reinterpret_cast<float*>(smem + kAclRedM);
-  float* red_l = reinterpret_cast<float*>(smem + kAclRedL);
   float* coef = reinterpret_cast<float*>(smem + kAclCoef);
   float* m_blk = reinterpret_cast<float*>(smem + kAclM);
   float* l_blk = reinterpret_cast<float*>(smem + kAclL);
   int* key_ok = reinterpret_cast<int*>(smem + kAclKeyOk);
+  const uint32_t bar = smem_u32addr(smem + kAclBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kAclBar + 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + kAclBar + 12);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (w == 0) tc_alloc(smem_u32addr(tmem_slot), kAclTmemCols);
 
   const int n_b = (int)min((int64_t)__ldg(len + b), cap);
   const size_t seq_row0 = (size_t)b * cap;
@@ -82,8 +124,8 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
   const int kk = tid >> 2, qq = tid & 3;
   const int j = r * kAclKeys + kk;  // position in the row's key list
   int kind = 0;                     // 0 none, 1 cache entry, 2 window row
-  uint4 cv[4];
-  uint2 sc8 = make_uint2(0u, 0u);
+  uint2 cv[8];                      // codes of the 16-dim groups 4m + qq, m = 0..7
+  uint4 sc[2];                      // the entry's 32 E4M3 bytes
 
   // ---- queries: heads 4w .. 4w+3 (lane: dims 16 lane .. 16 lane + 15); every load first
   uint32_t qlo[4][8];  // fp32 queries: the fp16 remainder, stored after the first S pass
@@ -118,10 +160,12 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
       if (pos >= n_b) set_dev_error(CSA2_ERR_BOUNDS);
       if (pos >= 0 && pos < n_b) {
         kind = 1;
-        const uint4* src = reinterpret_cast<const uint4*>(lat_codes + (seq_row0 + pos) * 256 + 64 * qq);
+        const uint2* src = reinterpret_cast<const uint2*>(lat_codes + (seq_row0 + pos) * 256) + qq;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cv[i] = __ldg(src + i);
-        sc8 = __ldg(reinterpret_cast<const uint2*>(lat_scales + (seq_row0 + pos) * 32 + 8 * qq));
+        for (int m = 0; m < 8; ++m) cv[m] = __ldg(src + 4 * m);
+        const uint4* ss = reinterpret_cast<const uint4*>(lat_scales + (seq_row0 + pos) * 32);
+        sc[0] = __ldg(ss);
+        sc[1] = __ldg(ss + 1);
       }
     } else if (j < k + W) {
       kind = 2;
@@ -148,152 +192,158 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
         o[i] = pack_half2(h0, h1);
         qlo[hh][i] = NPART == 2 ? pack_half2(y0 - h0, y1 - h1) : 0u;
       }
-      *reinterpret_cast<uint4*>(qs + swzv(h, 2 * lane)) = make_uint4(o[0], o[1], o[2], o[3]);
-      *reinterpret_cast<uint4*>(qs + swzv(h, 2 * lane + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+      {  // lanes 4..7 of each eight store their odd chunk first: distinct 16-byte positions
+        const bool sw = ((lane >> 2) & 1) != 0;
+        const uint4 lo4 = make_uint4(o[0], o[1], o[2], o[3]), hi4 = make_uint4(o[4], o[5], o[6], o[7]);
+        *reinterpret_cast<uint4*>(qs + acl_qidx(h, 2 * lane + (sw ? 1 : 0))) = sw ? hi4 : lo4;
+        *reinterpret_cast<uint4*>(qs + acl_qidx(h, 2 * lane + (sw ? 0 : 1))) = sw ? lo4 : hi4;
+      }
     }
   }
 
-  // ---- keys -> fp16 V rows (invalid keys: zero rows)
+  // ---- keys -> fp16 V rows (invalid keys: zero rows). Thread qq of a key takes the
+  // 16-dim groups 4m + qq: the eight lanes of one store (two keys x four threads) then
+  // write eight distinct 16-byte positions of the swizzled rows.
   if (kind == 1) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {  // 16 code bytes = 32 dims = 2 scale blocks
-      const uint32_t cw[4] = {cv[i].x, cv[i].y, cv[i].z, cv[i].w};
+    for (int m = 0; m < 8; ++m) {
+      const uint32_t sw = m < 4 ? (m == 0 ? sc[0].x : m == 1 ? sc[0].y : m == 2 ? sc[0].z : sc[0].w)
+                                : (m == 4 ? sc[1].x : m == 5 ? sc[1].y : m == 6 ? sc[1].z : sc[1].w);
+      const __half2 s2 = __float2half2_rn(e4m3_decode((sw >> (8 * qq)) & 0xFFu));  // scale of group 4m + qq
+      const uint32_t cw[2] = {cv[m].x, cv[m].y};
+      uint32_t o[8];
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const int sidx = 2 * i + hb;
-        const uint32_t sbyte = ((sidx < 4 ? sc8.x : sc8.y) >> (8 * (sidx & 3))) & 0xFFu;
-        const __half2 s2 = __float2half2_rn(e4m3_decode(sbyte));
-        uint32_t o[8];
+      for (int wv = 0; wv < 2; ++wv) {
 #pragma unroll
-        for (int wv = 0; wv < 2; ++wv) {
-          const uint32_t word = cw[2 * hb + wv];
-#pragma unroll
-          for (int by = 0; by < 4; ++by) {
-            const __half2_raw rr =
-                __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((word >> (8 * by)) & 0xFFu), __NV_E2M1);
-            const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&rr), s2);
-            o[4 * wv + by] = *reinterpret_cast<const uint32_t*>(&v);
-          }
+        for (int by = 0; by < 4; ++by) {
+          const __half2_raw rr =
+              __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((cw[wv] >> (8 * by)) & 0xFFu), __NV_E2M1);
+          const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&rr), s2);
+          o[4 * wv + by] = *reinterpret_cast<const uint32_t*>(&v);
         }
-        const int chunk = 16 * qq + 4 * i + 2 * hb;
-        *reinterpret_cast<uint4*>(vs + swzv(kk, chunk)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(vs + swzv(kk, chunk + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
+      const int chunk = 2 * (4 * m + qq);
+      *reinterpret_cast<uint4*>(vs + acl_vidx(kk, chunk)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(vs + acl_vidx(kk, chunk + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
     }
   } else if (kind == 2) {
-    const uint4* src = reinterpret_cast<const uint4*>(swa + ((size_t)b * W + (j - k)) * 512 + 128 * qq);
+    const uint4* src = reinterpret_cast<const uint4*>(swa + ((size_t)b * W + (j - k)) * 512);
 #pragma unroll 4
     for (int i = 0; i < 16; ++i) {
-      const uint4 v = __ldg(src + i);
+      const int chunk = 2 * (4 * (i >> 1) + qq) + (i & 1);
+      const uint4 v = __ldg(src + chunk);
       const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         o[e] = pack_half2(bf16_bits_to_float(vw[e] & 0xFFFFu), bf16_bits_to_float(vw[e] >> 16));
-      *reinterpret_cast<uint4*>(vs + swzv(kk, 16 * qq + i)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(vs + acl_vidx(kk, chunk)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   } else {
 #pragma unroll 4
-    for (int i = 0; i < 16; ++i) *reinterpret_cast<uint4*>(vs + swzv(kk, 16 * qq + i)) = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 16; ++i)
+      *reinterpret_cast<uint4*>(vs + acl_vidx(kk, 2 * (4 * (i >> 1) + qq) + (i & 1))) = make_uint4(0, 0, 0, 0);
   }
   if (qq == 0) key_ok[kk] = kind != 0 ? 1 : 0;
-  __syncthreads();
 
-  // ---- S = Q V^T: warp (mt, kg): heads 16mt .. 16mt+15, keys 32kg .. 32kg+31
-  const int mt = w & 3, kg = w >> 2;
-  float sacc[4][4];
-#pragma unroll
-  for (int jn = 0; jn < 4; ++jn) sacc[jn][0] = sacc[jn][1] = sacc[jn][2] = sacc[jn][3] = 0.f;
+  // ---- S^T = V Q^T on the tensor cores (tcgen05, M = 128 keys, N = 64 heads, K = 512
+  // in 32 steps): one thread issues, the accumulator lives in tensor memory
+  fence_proxy_async_smem();  // this thread's Q and V stores, for the tensor core's reads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 #pragma unroll
   for (int part = 0; part < NPART; ++part) {
     if (part == 1) {  // the fp16 remainder of fp32 queries replaces the first part
-      __syncthreads();
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) {
         const int h = 4 * w + hh;
-        *reinterpret_cast<uint4*>(qs + swzv(h, 2 * lane)) =
-            make_uint4(qlo[hh][0], qlo[hh][1], qlo[hh][2], qlo[hh][3]);
-        *reinterpret_cast<uint4*>(qs + swzv(h, 2 * lane + 1)) =
-            make_uint4(qlo[hh][4], qlo[hh][5], qlo[hh][6], qlo[hh][7]);
+        const bool sw = ((lane >> 2) & 1) != 0;
+        const uint4 lo4 = make_uint4(qlo[hh][0], qlo[hh][1], qlo[hh][2], qlo[hh][3]);
+        const uint4 hi4 = make_uint4(qlo[hh][4], qlo[hh][5], qlo[hh][6], qlo[hh][7]);
+        *reinterpret_cast<uint4*>(qs + acl_qidx(h, 2 * lane + (sw ? 1 : 0))) = sw ? hi4 : lo4;
+        *reinterpret_cast<uint4*>(qs + acl_qidx(h, 2 * lane + (sw ? 0 : 1))) = sw ? lo4 : hi4;
       }
+      fence_proxy_async_smem();
+      tc_fence_before();
       __syncthreads();
+      tc_fence_after();
     }
-    const uint32_t qb = smem_u32(qs), vb = smem_u32(vs);
+    if (tid == 0) {
+      const uint32_t vb = smem_u32addr(vs), qb = smem_u32addr(qs);
 #pragma unroll 4
-    for (int ks = 0; ks < 32; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(qb + swzv(16 * mt + (lane & 15), 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int key = 32 * kg + 16 * jj + (lane & 7) + ((lane >> 4) << 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(vb + swzv(key, 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
-        mma_f16(sacc[2 * jj], a0, a1, a2, a3, b0, b1);
-        mma_f16(sacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
+      for (int ks = 0; ks < 32; ++ks) {  // dims 16 ks .. 16 ks + 15: block ks/4, 32 bytes per step
+        const uint64_t da = smem_desc_sw128(vb + (ks >> 2) * (kAclKeys * 128) + (ks & 3) * 32);
+        const uint64_t db = smem_desc_sw128(qb + (ks >> 2) * (kAclHeads * 128) + (ks & 3) * 32);
+        tc_mma_f16_ss(tmem, da, db, kAclIDesc, (part > 0 || ks > 0) ? 1u : 0u);
       }
+      tc_commit(bar);
     }
+    mbar_wait_bounded(bar, (uint32_t)part, abort);  // the MMAs are done reading Q and V
+    tc_fence_after();
   }
 
-  // ---- softmax over this block's keys (heads h0 = 16mt + g, h1 = h0 + 8)
-  const int h0 = 16 * mt + g, h1 = h0 + 8;
+  // ---- logits: warp w reads keys 32(w%4) .. and heads 16(w/4) .. of S^T, scales and
+  // masks them, and stages them as S [head][key] (f32) over Q
   {
-    const float cf0 = coef[h0], cf1 = coef[h1];
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+    const int key = 32 * (w & 3) + lane, hc = 16 * (w >> 2);
+    uint32_t v[16];
+    tc_ld16(tmem + ((uint32_t)(32 * (w & 3)) << 16) + (uint32_t)hc, v);
+    tc_wait_ld();
+    const bool ok = key_ok[key] != 0;
+    float* sst = reinterpret_cast<float*>(smem + kAclSSt);
 #pragma unroll
-    for (int jn = 0; jn < 4; ++jn) {
-      const int key = 32 * kg + 8 * jn + 2 * t4;
-      const bool ok0 = key_ok[key] != 0, ok1 = key_ok[key + 1] != 0;
-      sacc[jn][0] = ok0 ? sacc[jn][0] * cf0 : -INFINITY;
-      sacc[jn][1] = ok1 ? sacc[jn][1] * cf0 : -INFINITY;
-      sacc[jn][2] = ok0 ? sacc[jn][2] * cf1 : -INFINITY;
-      sacc[jn][3] = ok1 ? sacc[jn][3] * cf1 : -INFINITY;
-      mx0 = fmaxf(mx0, fmaxf(sacc[jn][0], sacc[jn][1]));
-      mx1 = fmaxf(mx1, fmaxf(sacc[jn][2], sacc[jn][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    if (t4 == 0) {
-      red_m[kg * kAclHeads + h0] = mx0;
-      red_m[kg * kAclHeads + h1] = mx1;
-    }
-    __syncthreads();  // (also: every warp is done reading Q, so P may overwrite it)
-    float M0 = -INFINITY, M1 = -INFINITY;
+    for (int i = 0; i < 16; ++i) sst[(hc + i) * kAclKeys + key] = ok ? __uint_as_float(v[i]) * coef[hc + i] : -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (w == 0) {  // every read of tensor memory is done
+    tc_fence_after();
+    tc_dealloc(tmem, kAclTmemCols);
+  }
+
+  // ---- softmax over this block's keys: thread (h, seg) takes keys 16 seg .. 16 seg + 15
+  // of head h; the eight segments of a head are eight consecutive lanes
+  {
+    const int h = tid >> 3, seg = tid & 7;
+    const float4* sr = reinterpret_cast<const float4*>(smem + kAclSSt) + (h * kAclKeys + 16 * seg) / 4;
+    // read j takes keys 16 seg + 4 jj .., jj = (j + seg / 2) mod 4: the eight lanes
+    // of a read hit eight distinct 16-byte positions
+    float x[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      M0 = fmaxf(M0, red_m[i * kAclHeads + h0]);
-      M1 = fmaxf(M1, red_m[i * kAclHeads + h1]);
+    for (int j = 0; j < 4; ++j) {
+      const float4 t = sr[(j + (seg >> 1)) & 3];
+      x[4 * j] = t.x; x[4 * j + 1] = t.y; x[4 * j + 2] = t.z; x[4 * j + 3] = t.w;
     }
-    const float Z0 = M0 == -INFINITY ? 0.f : M0, Z1 = M1 == -INFINITY ? 0.f : M1;
-    float ls0 = 0.f, ls1 = 0.f;
+    float M = x[0];
 #pragma unroll
-    for (int jn = 0; jn < 4; ++jn) {
-      const int key = 32 * kg + 8 * jn + 2 * t4;
-      const __half2 p01 = __floats2half2_rn(exp2f(sacc[jn][0] - Z0), exp2f(sacc[jn][1] - Z0));
-      const __half2 p23 = __floats2half2_rn(exp2f(sacc[jn][2] - Z1), exp2f(sacc[jn][3] - Z1));
+    for (int i = 1; i < 16; ++i) M = fmaxf(M, x[i]);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float Z = M == -INFINITY ? 0.f : M;
+    float ls = 0.f;
+    unsigned char* ps = smem + kAclP;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int jj = (j + (seg >> 1)) & 3;  // keys 16 seg + 4 jj .. + 3
+      const __half2 p01 = __floats2half2_rn(exp2f(x[4 * j] - Z), exp2f(x[4 * j + 1] - Z));
+      const __half2 p23 = __floats2half2_rn(exp2f(x[4 * j + 2] - Z), exp2f(x[4 * j + 3] - Z));
       const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
-      ls0 += f01.x + f01.y;
-      ls1 += f23.x + f23.y;
-      *reinterpret_cast<__half2*>(qs + acl_pidx(h0, key >> 3) + (key & 7) * 2) = p01;
-      *reinterpret_cast<__half2*>(qs + acl_pidx(h1, key >> 3) + (key & 7) * 2) = p23;
+      ls += (f01.x + f01.y) + (f23.x + f23.y);
+      *reinterpret_cast<uint2*>(ps + acl_pidx(h, 2 * seg + (jj >> 1)) + (jj & 1) * 8) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&p01), *reinterpret_cast<const uint32_t*>(&p23));
     }
-    ls0 += __shfl_xor_sync(0xffffffffu, ls0, 1);
-    ls0 += __shfl_xor_sync(0xffffffffu, ls0, 2);
-    ls1 += __shfl_xor_sync(0xffffffffu, ls1, 1);
-    ls1 += __shfl_xor_sync(0xffffffffu, ls1, 2);
-    if (t4 == 0) {
-      red_l[kg * kAclHeads + h0] = ls0;
-      red_l[kg * kAclHeads + h1] = ls1;
-      if (kg == 0) {
-        m_blk[h0] = M0;
-        m_blk[h1] = M1;
-      }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    if (seg == 0) {
+      m_blk[h] = M;
+      l_blk[h] = ls;
     }
   }
   __syncthreads();
-  if (tid < kAclHeads) l_blk[tid] = red_l[tid] + red_l[kAclHeads + tid] + red_l[2 * kAclHeads + tid] +
-                                    red_l[3 * kAclHeads + tid];
+  const int mt = w & 3;
+  const int h0 = 16 * mt + g, h1 = h0 + 8;
 
   // ---- O = P V: warp (mt, dq): heads 16mt .., dims 128dq .. 128dq+127
   const int dq = w >> 2;
@@ -301,7 +351,7 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
 #pragma unroll
   for (int jn = 0; jn < 16; ++jn) oacc[jn][0] = oacc[jn][1] = oacc[jn][2] = oacc[jn][3] = 0.f;
   {
-    const uint32_t pb = smem_u32(qs), vb = smem_u32(vs);
+    const uint32_t pb = smem_u32(smem + kAclP), vb = smem_u32(vs);
 #pragma unroll 2
     for (int ks = 0; ks < kAclKeys / 16; ++ks) {
       uint32_t a0, a1, a2, a3;
@@ -310,7 +360,7 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + swzv(key, 16 * dq + 2 * jj + (lane >> 4)), b0, b1, b2, b3);
+        ldsm_x4_t(vb + acl_vidx(key, 16 * dq + 2 * jj + (lane >> 4)), b0, b1, b2, b3);
         mma_f16(oacc[2 * jj], a0, a1, a2, a3, b0, b1);
         mma_f16(oacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
       }
