@@ -8,8 +8,8 @@
 // token", "Troisiemement" (E2M1 values with an E4M3 scale per 16 channels; a
 // 128-token sliding window kept outside the global cache).
 //
-// Per block (512 threads, 16 warps; shared memory: Q 64 KB + V 128 KB; 64 columns of
-// tensor memory):
+// Per block (512 threads, 16 warps; shared memory: Q 64 KB + V 128 KB; 256 columns
+// of tensor memory):
 //  * thread t loads a quarter of key t/4 (64 code bytes, 8 E4M3 bytes) into
 //    registers at once, then the queries (per-head 2^s scaling as in the chunked
 //    form; fp32 queries as fp16 hi + lo, the lo part kept in registers) go to
@@ -20,8 +20,10 @@
 //    pass with the fp16 remainder) into tensor memory, and the warps read the
 //    logits back with tcgen05.ld;
 //  * softmax over the block's keys (base 2; eight lanes per head through a
-//    shared-memory copy of S), P rounded to fp16 and kept over the Q area;
-//  * O = P V: warp (mt, dq) owns heads 16mt.. and dims 128dq..;
+//    shared-memory copy of S), P rounded to fp16 and stored over the Q area;
+//  * O^T = V^T P^T on the tensor cores as well: V read in place as an MN-major
+//    operand, P (K-major) written by the softmax, four M = 128 blocks of dims into
+//    tensor memory, read back one dim per thread;
 //  * the unnormalised O, max and sum of every block are staged in its shared
 //    memory; after a cluster barrier block r merges heads [64r/C, 64(r+1)/C) of
 //    all C blocks (distributed shared memory: the weights in one round of remote
@@ -51,17 +53,18 @@ constexpr int kAclL = kAclM + kAclHeads * 4;              // [64] f32: this bloc
 constexpr int kAclKeyOk = kAclL + kAclHeads * 4;          // [128] i32
 constexpr int kAclBar = kAclKeyOk + kAclKeys * 4;         // mbarrier (8 B), tensor-memory base (4 B), abort (4 B)
 constexpr int kAclSmem = kAclBar + 16 + 1024;             // + slack to align the base to 1024 bytes
-constexpr int kAclTmemCols = 64;                          // S^T: 128 lanes (keys) x 64 columns (heads)
-// instruction descriptor, kind::f16: D f32, A = B = f16, both K-major, M = 128, N = 64
+// tensor memory: S^T (128 lanes = keys, columns 0..63 = heads), then O^T (four blocks
+// of 128 dims: lanes = dims, columns 64 mb .. 64 mb + 63 = heads)
+constexpr int kAclTmemCols = 256;
+// instruction descriptors, kind::f16: D f32, A = B = f16, M = 128, N = 64. S: both
+// operands K-major. O: A (V^T) MN-major, B (P^T) K-major.
 constexpr uint32_t kAclIDesc = (1u << 4) | ((uint32_t)(kAclHeads >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+constexpr uint32_t kAclIDescPV = kAclIDesc | (1u << 15);
 static_assert(kAclP + kAclHeads * kAclKeys * 2 <= kAclV, "S and P fit over Q");
 constexpr int kAclOPitch = 520;                           // floats per staged O row (bank spread)
 constexpr int kAclO = 0;                                  // [64][520] f32 over Q and V, after O = P V
 static_assert(kAclO + kAclHeads * kAclOPitch * 4 <= kAclRedM, "staged O fits over Q and V");
 static_assert((kAclMaxBlocks + 1) * kAclHeads * 4 <= kAclM - kAclRedM, "merge weights fit over RedM, RedL and Coef");
-
-// P [64 heads][128 keys] fp16: 16-byte chunk c of row h.
-__device__ __forceinline__ uint32_t acl_pidx(int h, int c) { return (uint32_t)(h * 256 + ((c ^ (h & 7)) << 4)); }
 
 // The tensor core's K-major, 128-byte-swizzled operand layout: 16-byte chunk c (dims
 // 8c .. 8c+7) of row r sits in the 64-dim block c/8, in row r of that block (128 B
@@ -73,6 +76,14 @@ __device__ __forceinline__ uint32_t acl_kidx(int r, int c, int rows) {
 }
 __device__ __forceinline__ uint32_t acl_vidx(int key, int c) { return acl_kidx(key, c, kAclKeys); }
 __device__ __forceinline__ uint32_t acl_qidx(int h, int c) { return acl_kidx(h, c, kAclHeads); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle, with an explicit leading-
+// dimension byte offset (the stride between 64-element swizzle atoms along M or N of
+// an MN-major operand) and the 1,024-byte stride between 8-row groups.
+__device__ __forceinline__ uint64_t smem_desc_sw128_lbo(uint32_t saddr, uint32_t lbo_bytes) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
 
 // D[tmem] (+)= A[smem descriptor] x B[smem descriptor], kind::f16.
 __device__ __forceinline__ void tc_mma_f16_ss(uint32_t d_taddr, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -297,11 +308,7 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
     for (int i = 0; i < 16; ++i) sst[(hc + i) * kAclKeys + key] = ok ? __uint_as_float(v[i]) * coef[hc + i] : -INFINITY;
   }
   tc_fence_before();
-  __syncthreads();
-  if (w == 0) {  // every read of tensor memory is done
-    tc_fence_after();
-    tc_dealloc(tmem, kAclTmemCols);
-  }
+  __syncthreads();  // every read of S^T is done: O^T may reuse its columns
 
   // ---- softmax over this block's keys: thread (h, seg) takes keys 16 seg .. 16 seg + 15
   // of head h; the eight segments of a head are eight consecutive lanes
@@ -331,7 +338,7 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
       const __half2 p23 = __floats2half2_rn(exp2f(x[4 * j + 2] - Z), exp2f(x[4 * j + 3] - Z));
       const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
       ls += (f01.x + f01.y) + (f23.x + f23.y);
-      *reinterpret_cast<uint2*>(ps + acl_pidx(h, 2 * seg + (jj >> 1)) + (jj & 1) * 8) =
+      *reinterpret_cast<uint2*>(ps + acl_qidx(h, 2 * seg + (jj >> 1)) + (jj & 1) * 8) =
           make_uint2(*reinterpret_cast<const uint32_t*>(&p01), *reinterpret_cast<const uint32_t*>(&p23));
     }
 #pragma unroll
@@ -341,45 +348,58 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
       l_blk[h] = ls;
     }
   }
+  // ---- O^T = V^T P^T on the tensor cores: M = 128 dims (four blocks), N = 64 heads,
+  // K = 128 keys in 8 steps. A = V read in place as an MN-major operand (dims run
+  // along its 128-byte rows; 64-dim atoms 16 KB apart, 8-key groups 1 KB apart); B = P,
+  // K-major (rows = heads).
+  fence_proxy_async_smem();  // this thread's P stores, for the tensor core's reads
+  tc_fence_before();
   __syncthreads();
-  const int mt = w & 3;
-  const int h0 = 16 * mt + g, h1 = h0 + 8;
-
-  // ---- O = P V: warp (mt, dq): heads 16mt .., dims 128dq .. 128dq+127
-  const int dq = w >> 2;
-  float oacc[16][4];
+  tc_fence_after();
+  if (tid == 0) {
+    const uint32_t vb = smem_u32addr(vs), pb = smem_u32addr(smem + kAclP);
 #pragma unroll
-  for (int jn = 0; jn < 16; ++jn) oacc[jn][0] = oacc[jn][1] = oacc[jn][2] = oacc[jn][3] = 0.f;
-  {
-    const uint32_t pb = smem_u32(smem + kAclP), vb = smem_u32(vs);
-#pragma unroll 2
-    for (int ks = 0; ks < kAclKeys / 16; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(pb + acl_pidx(16 * mt + (lane & 15), 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-      const int key = 16 * ks + (lane & 7) + (((lane >> 3) & 1) << 3);
+    for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + acl_vidx(key, 16 * dq + 2 * jj + (lane >> 4)), b0, b1, b2, b3);
-        mma_f16(oacc[2 * jj], a0, a1, a2, a3, b0, b1);
-        mma_f16(oacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
+      for (int ks = 0; ks < kAclKeys / 16; ++ks) {  // keys 16 ks .. 16 ks + 15
+        const uint64_t da = smem_desc_sw128_lbo(vb + 2 * mb * (kAclKeys * 128) + ks * 2048, kAclKeys * 128);
+        const uint64_t db = smem_desc_sw128(pb + (ks >> 2) * (kAclHeads * 128) + (ks & 3) * 32);
+        tc_mma_f16_ss(tmem + 64 * mb, da, db, kAclIDescPV, ks > 0 ? 1u : 0u);
       }
     }
+    tc_commit(bar);
+  }
+  mbar_wait_bounded(bar, (uint32_t)(NPART & 1), abort);  // the MMAs are done with P and V
+  tc_fence_after();
+  // warp w: dims 128 (w / 4) + 32 (w % 4) + lane, all 64 heads
+  float ov[64];
+  {
+    const uint32_t ta = tmem + ((uint32_t)(32 * (w & 3)) << 16) + (uint32_t)(64 * (w >> 2));
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t v[16];
+      tc_ld16(ta + 16 * q4, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ov[16 * q4 + i] = __uint_as_float(v[i]);
+    }
+    tc_wait_ld();
+  }
+  tc_fence_before();
+  __syncthreads();  // every read of tensor memory is done; P and V are free
+  if (w == 0) {
+    tc_fence_after();
+    tc_dealloc(tmem, kAclTmemCols);
   }
   // ---- merge: block r finishes heads [64r/C, 64(r+1)/C) of all C blocks. Every
   // block stages its unnormalised O over its own Q and V; after a cluster barrier
   // block r reads the max and sum of its heads from every block (one round of
   // remote loads into shared memory), then each thread loads the C partial rows
   // of its items with all loads in flight at once.
-  __syncthreads();  // every warp is done with P and V: stage O over them
   {
     float* os = reinterpret_cast<float*>(smem + kAclO);
+    const int d = 128 * (w >> 2) + 32 * (w & 3) + lane;
 #pragma unroll
-    for (int jn = 0; jn < 16; ++jn) {
-      const int d = 128 * dq + 8 * jn + 2 * t4;
-      *reinterpret_cast<float2*>(os + h0 * kAclOPitch + d) = make_float2(oacc[jn][0], oacc[jn][1]);
-      *reinterpret_cast<float2*>(os + h1 * kAclOPitch + d) = make_float2(oacc[jn][2], oacc[jn][3]);
-    }
+    for (int h = 0; h < kAclHeads; ++h) os[h * kAclOPitch + d] = ov[h];
   }
   cluster.sync();  // every block's O, max and sum are staged
   const int hb0 = r * kAclHeads / C, nh = (r + 1) * kAclHeads / C - hb0;
