@@ -59,6 +59,7 @@ _PROTOS = {
     "csa2_status_str": (C.c_char_p, [C.c_int]),
     "csa2_launch_count": (C.c_uint64, []),
     "csa2_set_scan_events": (None, [C.c_void_p, C.c_void_p]),
+    "csa2_selftest_wait_timeout": (C.c_int, [C.c_uint64, C.c_void_p]),
 }
 
 

@@ -300,12 +300,32 @@ void launch_attn(const void* q, csa2_dtype dt, int H, float scale, const csa2_ca
   g_launches += 1;
 }
 
+// One thread waits, with the kernels' bounded wait and the given budget, on an
+// mbarrier that nothing ever arrives at: the wait runs out, records
+// CSA2_ERR_TIMEOUT in the device status word and the kernel returns.
+__global__ void k_selftest_wait(uint64_t budget_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32addr(&bar);
+  mbar_init(b, 1);
+  abort_flag = 0;
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  mbar_wait_bounded_ns(b, 0u, &abort_flag, budget_ns);
+}
+
 }  // namespace
 }  // namespace csa2
 
 using namespace csa2;
 
 extern "C" {
+
+csa2_status csa2_selftest_wait_timeout(uint64_t budget_ns, csa2_stream_t stream) {
+  if (budget_ns > 1000000000ull) return CSA2_ERR_ARG;
+  k_selftest_wait<<<1, 32, 0, (cudaStream_t)stream>>>(budget_ns);
+  return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+}
 
 csa2_status kv_quant_append(const void* lat, const void* ikey, csa2_dtype in_dtype, int32_t T, int32_t ratio,
                             const float* w0_lat, const float* w1_lat, const float* w0_idx, const float* w1_idx,

@@ -375,9 +375,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of the given parity; false after ~1 s (error recorded) or
-// when another thread of the block has given up (*abort set).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
+// Wait for the phase of the given parity; false after about budget_ns (error
+// recorded) or when another thread of the block has given up (*abort set).
+__device__ __forceinline__ bool mbar_wait_bounded_ns(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                     uint64_t budget_ns) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -386,13 +387,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
       const uint64_t now = globaltimer_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > 1000000000ull) {
+      } else if (now - t0 > budget_ns) {
         set_dev_error(CSA2_ERR_TIMEOUT);
         *abort = 1;
         return false;
       }
     }
   }
+}
+
+// The kernels' waits: about one second.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return mbar_wait_bounded_ns(bar, parity, abort, 1000000000ull);
 }
 
 __device__ __forceinline__ void tma_load_rows(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar,

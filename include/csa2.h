@@ -265,6 +265,20 @@ CSA2_API uint64_t csa2_launch_count(void);
  */
 CSA2_API void csa2_set_scan_events(void* before, void* after);
 
+/*
+ * csa2_selftest_wait_timeout -- test hook for the failure detection.
+ *
+ * Not an operation of the method (the pages have no counterpart). Launches one
+ * block on ``stream`` in which one thread waits, with the same bounded mbarrier
+ * wait as the streaming kernels but a limit of ``budget_ns`` nanoseconds, on a
+ * barrier that nothing ever arrives at. The wait runs out, records
+ * CSA2_ERR_TIMEOUT in the device status word and the kernel returns; the next
+ * csa2_sync_status() on that stream reports it (and clears it). Nothing faults,
+ * traps or hangs. budget_ns <= 1e9, else CSA2_ERR_ARG; CSA2_ERR_CUDA if the
+ * launch fails.
+ */
+CSA2_API csa2_status csa2_selftest_wait_timeout(uint64_t budget_ns, csa2_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
