@@ -244,7 +244,7 @@ def run_ours(args, rank, world, local):
 
     def step(ev=None):
         """One decode step: append this step's token to every sequence, then the Full
-        layer (indexer scan with its fused Top-512, gather + attention)."""
+        layer (indexer scan, cluster Top-512, gather + attention)."""
         K.kv_quant_append(tok_lat, tok_key, 1, cache)
         if ev is not None:
             K.set_scan_events(ev[0], ev[1])
