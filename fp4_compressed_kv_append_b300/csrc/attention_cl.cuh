@@ -101,16 +101,15 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
                  const uint8_t* __restrict__ lat_scales, const int32_t* __restrict__ len, int64_t cap,
                  const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int W, int H,
                  float* __restrict__ out) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  extern __shared__ __align__(1024) unsigned char acl_smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+      (reinterpret_cast<uintptr_t>(acl_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int r = (int)cluster.block_rank();
   const int hg = blockIdx.x / C, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int g = lane >> 2, t4 = lane & 3;
   unsigned char* qs = smem + kAclQ;
   unsigned char* vs = smem + kAclV;
   float* coef = reinterpret_cast<float*>(smem + kAclCoef);
