@@ -237,7 +237,10 @@ def run_ours(args, rank, world, local):
     n_graphs = max(1, -(-args.steps // STEPS_PER_GRAPH))
     K_steps = n_graphs * STEPS_PER_GRAPH
     warm_graphs = max(1, -(-args.warmup // STEPS_PER_GRAPH))
-    total_appends = (warm_graphs + n_graphs + 4) * STEPS_PER_GRAPH + args.e2e_steps + 16
+    # appends: device-timed graphs (+ warm-up and eager steps), then the e2e run's eager
+    # warm-up, one untimed and the timed graph replays
+    e2e_graphs = max(1, -(-args.e2e_steps // STEPS_PER_GRAPH))
+    total_appends = (warm_graphs + n_graphs + 4) * STEPS_PER_GRAPH + (e2e_graphs + 2) * STEPS_PER_GRAPH
     wl = CF.DecodeWorkload(c, extra=total_appends)
     cache = wl.cache
     tok_lat, tok_key = WL.new_token(c["seed"], 0, B, device="cuda")
@@ -336,41 +339,89 @@ def run_ours(args, rank, world, local):
 
 
 def e2e_run(args, K, CF, wl, c, tok_lat, tok_key):
-    """Same step through csa2_decode_step with pinned host inputs/outputs copied every step."""
+    """The same step through the public API (kv_quant_append + csa2_decode_step) with
+    pinned host buffers: every step copies its inputs (q, q_idx, w, the new token)
+    host -> device and reads its attention output device -> host. The steps run in
+    order on one compute stream (each step's append before its scan); the copies run
+    on their own two streams into and out of two sets of device buffers, so a step's
+    copies overlap the neighbouring steps' kernels (a serving loop's double buffering).
+    """
     B, H = c["B"], c["H"]
-    layer = wl.layers[0]
-    h_q = layer.q.cpu().pin_memory()
-    h_qi = layer.q_idx.cpu().pin_memory()
-    h_w = layer.w_idx.cpu().pin_memory()
+    L0 = wl.layers[0]
+    h_q = L0.q.cpu().pin_memory()
+    h_qi = L0.q_idx.cpu().pin_memory()
+    h_w = L0.w_idx.cpu().pin_memory()
     h_tl, h_tk = tok_lat.cpu().pin_memory(), tok_key.cpu().pin_memory()
-    h_out = torch.empty(B, H, 512, dtype=torch.float32).pin_memory()
-    d_tl, d_tk = torch.empty_like(tok_lat), torch.empty_like(tok_key)
-    step = wl.step
+    n_slots = 2
+    slots = []
+    for _ in range(n_slots):
+        d = dict(q=torch.empty_like(L0.q), qi=torch.empty_like(L0.q_idx), w=torch.empty_like(L0.w_idx),
+                 tl=torch.empty_like(tok_lat), tk=torch.empty_like(tok_key), out=torch.empty_like(L0.out),
+                 h_out=torch.empty(B, H, 512, dtype=torch.float32).pin_memory())
+        layer = K.Layer(L0.mode, d["q"], d["out"], cache=L0.cache, q_idx=d["qi"], w_idx=d["w"], pool=L0.pool,
+                        idx_out=torch.empty_like(L0.idx_out))
+        d["step"] = K.DecodeStep([layer], CF.TOPK, ws=wl.step.ws)  # steps are in order: one workspace
+        slots.append(d)
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_qi, h_w, h_tl, h_tk))
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = slots[0]["h_out"].numel() * 4
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(n_slots)]
+    ev_comp = [torch.cuda.Event() for _ in range(n_slots)]
+    ev_out = [torch.cuda.Event() for _ in range(n_slots)]
 
-    def one():
-        layer.q.copy_(h_q, non_blocking=True)
-        layer.q_idx.copy_(h_qi, non_blocking=True)
-        layer.w_idx.copy_(h_w, non_blocking=True)
-        d_tl.copy_(h_tl, non_blocking=True)
-        d_tk.copy_(h_tk, non_blocking=True)
-        K.kv_quant_append(d_tl, d_tk, 1, wl.cache)
-        step()
-        h_out.copy_(layer.out, non_blocking=True)
+    def one(i):
+        j = i % n_slots
+        d = slots[j]
+        with torch.cuda.stream(s_in):
+            if i >= n_slots:
+                s_in.wait_event(ev_comp[j])  # the slot's previous step has consumed its inputs
+            d["q"].copy_(h_q, non_blocking=True)
+            d["qi"].copy_(h_qi, non_blocking=True)
+            d["w"].copy_(h_w, non_blocking=True)
+            d["tl"].copy_(h_tl, non_blocking=True)
+            d["tk"].copy_(h_tk, non_blocking=True)
+            ev_in[j].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev_in[j])
+            if i >= n_slots:
+                s_comp.wait_event(ev_out[j])  # the slot's previous output has been read out
+            K.kv_quant_append(d["tl"], d["tk"], 1, wl.cache)
+            d["step"]()
+            ev_comp[j].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[j])
+            d["h_out"].copy_(d["out"], non_blocking=True)
+            ev_out[j].record(s_out)
 
-    for _ in range(3):
-        one()
+    for i in range(2 * n_slots):  # eager warm-up of the same sequence
+        one(i)
+    torch.cuda.synchronize()
+    # STEPS_PER_GRAPH steps per CUDA graph (copies, appends and steps as captured
+    # nodes on the three streams); replays are serialised on one stream
+    cap = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for s in (s_in, s_comp, s_out):
+            s.wait_stream(cap)
+        for i in range(STEPS_PER_GRAPH):
+            one(i)
+        for s in (s_in, s_comp, s_out):
+            cap.wait_stream(s)
+    n_rep = max(1, -(-args.e2e_steps // STEPS_PER_GRAPH))
+    g.replay()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        one()
+    for _ in range(n_rep):
+        g.replay()
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     assert K.sync_status() == 0
-    return {"value": B * args.e2e_steps / dt, "unit": "queries/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "api": "kv_quant_append + csa2_decode_step, pinned host buffers",
-            "steps": args.e2e_steps}
+    steps = n_rep * STEPS_PER_GRAPH
+    return {"value": B * steps / dt, "unit": "queries/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "api": "kv_quant_append + csa2_decode_step, pinned host buffers, copies double-buffered on "
+                   f"their own streams, {STEPS_PER_GRAPH} steps per CUDA graph",
+            "steps": steps}
 
 
 def main():
