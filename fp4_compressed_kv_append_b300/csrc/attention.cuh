@@ -130,6 +130,7 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
               const uint8_t* __restrict__ lat_scales, const int32_t* __restrict__ len, int64_t cap,
               const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int W, int H,
               float* __restrict__ out) {
+  pdl_wait_and_release();
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* vs = smem + kAttnV;
   float* spart = reinterpret_cast<float*>(smem + kAttnSPart);

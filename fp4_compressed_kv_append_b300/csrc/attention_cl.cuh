@@ -101,6 +101,7 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
                  const uint8_t* __restrict__ lat_scales, const int32_t* __restrict__ len, int64_t cap,
                  const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int W, int H,
                  float* __restrict__ out) {
+  pdl_wait_and_release();
   extern __shared__ __align__(1024) unsigned char acl_smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(acl_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

@@ -120,6 +120,17 @@ __device__ __forceinline__ unsigned long long topk_key(float s, uint32_t slot) {
   return ((unsigned long long)float_order_key(s) << 32) | (unsigned long long)(0xFFFFFFFFu - slot);
 }
 
+// ---------------------------------------------------------------- launch ordering
+// Programmatic dependent launch: a kernel waits for the kernel before it in the
+// stream (its completion and memory) before touching global memory, then lets the
+// kernel after it launch. A kernel launched behind a kernel that never triggers
+// starts after that kernel ends, as without these calls; without a programmatic
+// dependency the wait returns at once.
+__device__ __forceinline__ void pdl_wait_and_release() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint32_t smem_u32addr(const void* p) { return smem_u32(p); }

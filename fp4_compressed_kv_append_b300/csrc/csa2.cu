@@ -32,6 +32,47 @@ void record_hook_event(cudaEvent_t ev, cudaStream_t s) {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Kernels may launch while the kernel before them in the stream finishes (each
+// kernel waits for it with griddepcontrol.wait before touching global memory);
+// CSA2_PDL=0 launches them one after another instead (read once).
+bool pdl_enabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("CSA2_PDL");
+    v = (e && strcmp(e, "0") == 0) ? 0 : 1;
+  }
+  return v == 1;
+}
+
+// Launch `kern` on `s` with programmatic stream serialization (when enabled) and,
+// when cluster_x > 0, a cluster of cluster_x blocks along x.
+template <typename... KArgs, typename... Args>
+void launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, unsigned cluster_x,
+              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  unsigned n = 0;
+  if (pdl_enabled()) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 0) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster_x;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 inline csa2_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
@@ -65,16 +106,16 @@ void launch_append(const void* lat, const void* ikey, csa2_dtype dt, int T, int 
   const int n_new = T / ratio;
   const dim3 grid((n_new + kAppendWarps - 1) / kAppendWarps, c.batch);
   if (dt == CSA2_F32)
-    k_quant_append<float><<<grid, kAppendWarps * 32, 0, s>>>(
-        (const float*)lat, (const float*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes, c.lat_scales,
-        c.idx_codes, c.idx_scales, c.len, c.cap, n_new);
+    launch_k(k_quant_append<float>, grid, dim3(kAppendWarps * 32), 0, s, 0u, (const float*)lat,
+             (const float*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes, c.lat_scales, c.idx_codes,
+             c.idx_scales, c.len, c.cap, n_new);
   else
-    k_quant_append<uint16_t><<<grid, kAppendWarps * 32, 0, s>>>(
-        (const uint16_t*)lat, (const uint16_t*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes,
-        c.lat_scales, c.idx_codes, c.idx_scales, c.len, c.cap, n_new);
+    launch_k(k_quant_append<uint16_t>, grid, dim3(kAppendWarps * 32), 0, s, 0u, (const uint16_t*)lat,
+             (const uint16_t*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes, c.lat_scales, c.idx_codes,
+             c.idx_scales, c.len, c.cap, n_new);
   g_launches += 1;
   if (grid.x > 1) {  // several blocks per sequence: advance len once they are all done
-    k_bump_len<<<(c.batch + 255) / 256, 256, 0, s>>>(c.len, c.batch, c.cap, n_new);
+    launch_k(k_bump_len, dim3((c.batch + 255) / 256), dim3(256), 0, s, 0u, c.len, c.batch, c.cap, n_new);
     g_launches += 1;
   }
 }
@@ -103,7 +144,7 @@ void launch_scan_gather(const ScanArgs& a, cudaStream_t s) {
   const int64_t want = (a.total_tiles + kScanWarps - 1) / kScanWarps;  // >= 1 tile per warp
   const int64_t full = (int64_t)sm_count() * per_sm;
   const int grid = (int)(want < full ? want : full);
-  k_indexer_scan_gather<NPART><<<grid, kScanThreads, 0, s>>>(a);
+  launch_k(k_indexer_scan_gather<NPART>, dim3(grid), dim3(kScanThreads), 0, s, 0u, a);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -147,7 +188,7 @@ void launch_scan_tma(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s)
   }
   const int64_t full = (int64_t)sm_count() * kTmaBlocksPerSM;
   const int grid = (int)(a.total_tiles < full ? a.total_tiles : full);
-  k_indexer_scan_tma<NPART><<<grid, kTmaThreads, kTmaSmem, s>>>(m, a);
+  launch_k(k_indexer_scan_tma<NPART>, dim3(grid), dim3(kTmaThreads), kTmaSmem, s, 0u, m, a);
 }
 
 template <int NPART>
@@ -165,7 +206,7 @@ void launch_scan_tc(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s) 
   }
   const int64_t full = (int64_t)sm_count() * per_sm;
   const int grid = (int)(a.total_tiles < full ? a.total_tiles : full);
-  k_indexer_scan_tc<NPART><<<grid, kTcThreads, S::Smem, s>>>(m, a);
+  launch_k(k_indexer_scan_tc<NPART>, dim3(grid), dim3(kTcThreads), S::Smem, s, 0u, m, a);
 }
 
 // Which streaming scan runs: the mma.sync form unless CSA2_SCAN_KERNEL=tc asks for
@@ -233,7 +274,8 @@ void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, c
     cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
     attr_set = true;
   }
-  k_topk<<<dim3(kTopkCluster, batch), kTopkThreads, kTopkSmem, s>>>(scores, stride, n, cand, k, out);
+  launch_k(k_topk, dim3(kTopkCluster, batch), dim3(kTopkThreads), kTopkSmem, s, 0u, scores, stride, n, cand, k,
+           out);
   g_launches += 1;
 }
 
@@ -245,8 +287,8 @@ void launch_attn_t(const void* q, csa2_dtype dt, int H, float scale, const csa2_
     cudaFuncSetAttribute(k_sparse_attn<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
     attr_set = true;
   }
-  k_sparse_attn<NPART><<<dim3(2 * (H / kAttnHeads), c.batch), kAttnThreads, kAttnSmem, s>>>(
-      q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H, out);
+  launch_k(k_sparse_attn<NPART>, dim3(2 * (H / kAttnHeads), c.batch), dim3(kAttnThreads), kAttnSmem, s, 0u, q,
+           (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H, out);
 }
 
 // Key-split form: one cluster of ceil((k + W) / 128) blocks per (sequence, 64 heads).
@@ -259,20 +301,9 @@ void launch_attn_cl(const void* q, csa2_dtype dt, int H, float scale, const csa2
     attr_set = true;
   }
   const int C = (k + W + kAclKeys - 1) / kAclKeys;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(C * (H / kAclHeads)), (unsigned)c.batch, 1);
-  cfg.blockDim = dim3(kAclThreads, 1, 1);
-  cfg.dynamicSmemBytes = kAclSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = (unsigned)C;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, k_sparse_attn_cl<NPART>, q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap,
-                     idx, k, swa, W, H, out);
+  launch_k(k_sparse_attn_cl<NPART>, dim3((unsigned)(C * (H / kAclHeads)), (unsigned)c.batch), dim3(kAclThreads),
+           kAclSmem, s, (unsigned)C, q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H,
+           out);
 }
 
 // The key-split form covers 64-head groups and up to 1,024 keys per row; the

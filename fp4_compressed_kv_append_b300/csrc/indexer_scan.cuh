@@ -258,6 +258,7 @@ __device__ __forceinline__ float scan_m16(const uint32_t (&wl)[4], const uint32_
 // 32-entry tile ahead.
 template <int NPART>
 __global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan_gather(const ScanArgs a) {
+  pdl_wait_and_release();
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int64_t gw = (int64_t)blockIdx.x * kScanWarps + (threadIdx.x >> 5);
   const int64_t nw = (int64_t)gridDim.x * kScanWarps;
@@ -422,6 +423,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 template <int NPART>
 __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSM)
 k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a) {
+  pdl_wait_and_release();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

@@ -179,6 +179,7 @@ __device__ __forceinline__ void tc_setup_q(int b, const TmaScanArgs& a, int t, i
 template <int NPART>
 __global__ void __launch_bounds__(kTcThreads, 2)
 k_indexer_scan_tc(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a) {
+  pdl_wait_and_release();
   using S = TcShape<NPART>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(

@@ -125,6 +125,7 @@ k_quant_append(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
                uint8_t* __restrict__ lat_codes, uint8_t* __restrict__ lat_scales,
                uint8_t* __restrict__ idx_codes, uint8_t* __restrict__ idx_scales,
                int32_t* __restrict__ len, int64_t cap, int n_new) {
+  pdl_wait_and_release();
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
   const int b = blockIdx.y;
@@ -144,6 +145,7 @@ k_quant_append(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
 
 // Advance len[b] by n_new after an append (refused appends leave len unchanged).
 __global__ void k_bump_len(int32_t* len, int batch, int64_t cap, int n_new) {
+  pdl_wait_and_release();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < batch) {
     const int64_t l = len[b];

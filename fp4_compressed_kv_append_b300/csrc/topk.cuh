@@ -298,6 +298,7 @@ __device__ void rx_list_select(const uint32_t* lkey, uint32_t c, uint32_t need, 
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 2)
 k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ nvec,
        const int32_t* __restrict__ cand, int k, int32_t* __restrict__ out) {
+  pdl_wait_and_release();
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char smem_raw[];
