@@ -133,13 +133,35 @@ int sm_count() {
   return cached[dev];
 }
 
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  return dev;
+}
+
+// Raise Kern's dynamic shared-memory limit to `bytes`, once per device (function
+// attributes belong to the device's context).
+template <auto Kern>
+void ensure_max_smem(int bytes) {
+  static std::atomic<int> done[kMaxDevices];
+  const int dev = current_device();
+  if (done[dev].load(std::memory_order_acquire)) return;
+  cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  done[dev].store(1, std::memory_order_release);
+}
+
 template <int NPART>
 void launch_scan_gather(const ScanArgs& a, cudaStream_t s) {
-  static int per_sm = 0;
+  static std::atomic<int> per_sm_of[kMaxDevices];  // resident blocks per SM, per device
+  const int dev = current_device();
+  int per_sm = per_sm_of[dev].load(std::memory_order_relaxed);
   if (per_sm == 0) {
     int occ = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_indexer_scan_gather<NPART>, kScanThreads, 0);
     per_sm = occ > 0 ? occ : 1;
+    per_sm_of[dev].store(per_sm, std::memory_order_relaxed);
   }
   const int64_t want = (a.total_tiles + kScanWarps - 1) / kScanWarps;  // >= 1 tile per warp
   const int64_t full = (int64_t)sm_count() * per_sm;
@@ -181,11 +203,7 @@ bool make_codes_map(CUtensorMap* m, const uint8_t* codes, int64_t rows) {
 
 template <int NPART>
 void launch_scan_tma(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(k_indexer_scan_tma<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem);
-    attr_set = true;
-  }
+  ensure_max_smem<k_indexer_scan_tma<NPART>>(kTmaSmem);
   const int64_t full = (int64_t)sm_count() * kTmaBlocksPerSM;
   const int grid = (int)(a.total_tiles < full ? a.total_tiles : full);
   launch_k(k_indexer_scan_tma<NPART>, dim3(grid), dim3(kTmaThreads), kTmaSmem, s, 0u, m, a);
@@ -194,15 +212,17 @@ void launch_scan_tma(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s)
 template <int NPART>
 void launch_scan_tc(const CUtensorMap& m, const TmaScanArgs& a, cudaStream_t s) {
   using S = TcShape<NPART>;
-  static int per_sm = 0;
+  ensure_max_smem<k_indexer_scan_tc<NPART>>(S::Smem);
+  // two blocks per SM: their 256-column tensor-memory allocations fill the SM's 512
+  // columns, and registers (96 x 320 per block) and shared memory allow two
+  static std::atomic<int> per_sm_of[kMaxDevices];
+  const int dev = current_device();
+  int per_sm = per_sm_of[dev].load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    cudaFuncSetAttribute(k_indexer_scan_tc<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::Smem);
-    // two blocks per SM: their 256-column tensor-memory allocations fill the SM's 512
-    // columns, and registers (96 x 320 per block) and shared memory allow two
-    int dev = 0, smem_sm = 0;
-    cudaGetDevice(&dev);
+    int smem_sm = 0;
     cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
     per_sm = smem_sm >= 2 * (S::Smem + 1024) ? 2 : 1;
+    per_sm_of[dev].store(per_sm, std::memory_order_relaxed);
   }
   const int64_t full = (int64_t)sm_count() * per_sm;
   const int grid = (int)(a.total_tiles < full ? a.total_tiles : full);
@@ -269,11 +289,7 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
 
 void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,
                  int32_t* out, int batch, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
-    attr_set = true;
-  }
+  ensure_max_smem<k_topk>((int)kTopkSmem);
   launch_k(k_topk, dim3(kTopkCluster, batch), dim3(kTopkThreads), kTopkSmem, s, 0u, scores, stride, n, cand, k,
            out);
   g_launches += 1;
@@ -282,11 +298,7 @@ void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, c
 template <int NPART>
 void launch_attn_t(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
                    int k, const uint16_t* swa, int W, float* out, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(k_sparse_attn<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-    attr_set = true;
-  }
+  ensure_max_smem<k_sparse_attn<NPART>>(kAttnSmem);
   launch_k(k_sparse_attn<NPART>, dim3(2 * (H / kAttnHeads), c.batch), dim3(kAttnThreads), kAttnSmem, s, 0u, q,
            (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H, out);
 }
@@ -295,11 +307,7 @@ void launch_attn_t(const void* q, csa2_dtype dt, int H, float scale, const csa2_
 template <int NPART>
 void launch_attn_cl(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
                     int k, const uint16_t* swa, int W, float* out, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(k_sparse_attn_cl<NPART>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAclSmem);
-    attr_set = true;
-  }
+  ensure_max_smem<k_sparse_attn_cl<NPART>>(kAclSmem);
   const int C = (k + W + kAclKeys - 1) / kAclKeys;
   launch_k(k_sparse_attn_cl<NPART>, dim3((unsigned)(C * (H / kAclHeads)), (unsigned)c.batch), dim3(kAclThreads),
            kAclSmem, s, (unsigned)C, q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H,
