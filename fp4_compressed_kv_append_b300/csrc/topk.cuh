@@ -495,7 +495,13 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
         // which finishes alone (each block reserves its run of the list with one
         // remote atomic and writes it in slot order)
         uint32_t own = 0;
-        rx_visit(R, keys4, vbits, [&](uint32_t, uint32_t key) { own += key >= blo; });
+        unsigned long long qmask = 0;  // kept runs: the run's slots that qualify
+        rx_visit(R, keys4, vbits, [&](uint32_t sl, uint32_t key) {
+          if (key >= blo) {
+            ++own;
+            if (R.kept) qmask |= 1ull << (sl - R.s_begin);
+          }
+        });
         uint32_t cnt_r;
         const uint32_t at0 = block_excl_scan(own, sh, &cnt_r);
         if (tid == 0) {
@@ -509,13 +515,23 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
         uint32_t at = sh.bc[3] + at0;
         uint32_t* lkey0 = cluster.map_shared_rank(lkey, 0u);
         uint32_t* lslot0 = cluster.map_shared_rank(lslot, 0u);
-        rx_visit(R, keys4, vbits, [&](uint32_t s, uint32_t key) {
-          if (key >= blo) {
-            lkey0[at] = key;
-            lslot0[at] = s;
+        if (R.kept) {  // only the qualifying slots, in slot order
+          while (qmask) {
+            const int bi = __ffsll((long long)qmask) - 1;
+            qmask &= qmask - 1;
+            lkey0[at] = reinterpret_cast<const uint32_t*>(keys4 + rx_kidx((uint32_t)bi >> 2, tid))[bi & 3];
+            lslot0[at] = R.s_begin + (uint32_t)bi;
             ++at;
           }
-        });
+        } else {
+          rx_visit(R, keys4, vbits, [&](uint32_t s, uint32_t key) {
+            if (key >= blo) {
+              lkey0[at] = key;
+              lslot0[at] = s;
+              ++at;
+            }
+          });
+        }
         cluster.sync();  // the last cluster barrier: only block 0 goes on
         if (rank != 0) return;
         const uint32_t cl = sh.list_n;
