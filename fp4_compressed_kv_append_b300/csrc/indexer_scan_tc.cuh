@@ -4,9 +4,9 @@
 // indexer key scores positions) and section "Cles d'indexeur" (eq. 68: E2M1 with an
 // E8M0 scale per 32 channels).
 //
-// Same ring of shared-memory stages as the mma.sync form (a producer warp streams
-// 128-entry TMA boxes of codes, 64-byte swizzle, and their E8M0 bytes); the rest
-// is per entry:
+// A ring of shared-memory stages like the mma.sync form's, here of 128 entries (a
+// producer warp streams one TMA box of codes, 64-byte swizzle, and their E8M0 bytes
+// per stage); the rest is per entry:
 //  * two groups of four converter warps take the stages in turn; thread r of a
 //    group owns entry r of its stage (TMEM lane r): it turns the entry's 64 code
 //    bytes into 128 fp16 values (exact) and writes them to an A buffer in tensor
