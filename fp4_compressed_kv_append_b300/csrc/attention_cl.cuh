@@ -100,8 +100,7 @@ __global__ void __launch_bounds__(kAclThreads, 1)
 k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uint8_t* __restrict__ lat_codes,
                  const uint8_t* __restrict__ lat_scales, const int32_t* __restrict__ len, int64_t cap,
                  const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int W, int H,
-                 float* __restrict__ out) {
-  pdl_wait_and_release();
+                 float* __restrict__ out, int q_early) {
   extern __shared__ __align__(1024) unsigned char acl_smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(acl_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -125,9 +124,11 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  if (w == 0) tc_alloc(smem_u32addr(tmem_slot), kAclTmemCols);
-
-  const int n_b = (int)min((int64_t)__ldg(len + b), cap);
+  // q_early (set by the decode step when the kernel before this one is its own Top-k,
+  // which does not write the queries, and every kernel before that has completed by
+  // the time this one starts): the queries are loaded and staged before waiting for
+  // the Top-k. Otherwise everything waits for the previous kernel first.
+  if (!q_early) pdl_wait_and_release();
   const size_t seq_row0 = (size_t)b * cap;
 
   // ---- this thread's quarter of key kk (dims 128qq .. 128qq+127): codes and scales,
@@ -166,21 +167,25 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
         }
       }
     }
-    if (j < k) {
-      const int pos = idx ? __ldg(idx + (size_t)b * k + j) : -1;
-      if (pos >= n_b) set_dev_error(CSA2_ERR_BOUNDS);
-      if (pos >= 0 && pos < n_b) {
-        kind = 1;
-        const uint2* src = reinterpret_cast<const uint2*>(lat_codes + (seq_row0 + pos) * 256) + qq;
+    auto load_keys = [&]() {
+      const int n_b = (int)min((int64_t)__ldg(len + b), cap);
+      if (j < k) {
+        const int pos = idx ? __ldg(idx + (size_t)b * k + j) : -1;
+        if (pos >= n_b) set_dev_error(CSA2_ERR_BOUNDS);
+        if (pos >= 0 && pos < n_b) {
+          kind = 1;
+          const uint2* src = reinterpret_cast<const uint2*>(lat_codes + (seq_row0 + pos) * 256) + qq;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) cv[m] = __ldg(src + 4 * m);
-        const uint4* ss = reinterpret_cast<const uint4*>(lat_scales + (seq_row0 + pos) * 32);
-        sc[0] = __ldg(ss);
-        sc[1] = __ldg(ss + 1);
+          for (int m = 0; m < 8; ++m) cv[m] = __ldg(src + 4 * m);
+          const uint4* ss = reinterpret_cast<const uint4*>(lat_scales + (seq_row0 + pos) * 32);
+          sc[0] = __ldg(ss);
+          sc[1] = __ldg(ss + 1);
+        }
+      } else if (j < k + W) {
+        kind = 2;
       }
-    } else if (j < k + W) {
-      kind = 2;
-    }
+    };
+    if (!q_early) load_keys();  // in flight while the queries are scaled
 #pragma unroll
     for (int hh = 0; hh < 4; ++hh) {
       const int h = 4 * w + hh;
@@ -210,7 +215,12 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
         *reinterpret_cast<uint4*>(qs + acl_qidx(h, 2 * lane + (sw ? 0 : 1))) = sw ? lo4 : hi4;
       }
     }
+    if (q_early) {
+      pdl_wait_and_release();  // the selected indices (and the cache) are ready from here on
+      load_keys();
+    }
   }
+  if (w == 0) tc_alloc(smem_u32addr(tmem_slot), kAclTmemCols);
 
   // ---- keys -> fp16 V rows (invalid keys: zero rows). Thread qq of a key takes the
   // 16-dim groups 4m + qq: the eight lanes of one store (two keys x four threads) then

@@ -306,12 +306,12 @@ void launch_attn_t(const void* q, csa2_dtype dt, int H, float scale, const csa2_
 // Key-split form: one cluster of ceil((k + W) / 128) blocks per (sequence, 64 heads).
 template <int NPART>
 void launch_attn_cl(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
-                    int k, const uint16_t* swa, int W, float* out, cudaStream_t s) {
+                    int k, const uint16_t* swa, int W, float* out, int q_early, cudaStream_t s) {
   ensure_max_smem<k_sparse_attn_cl<NPART>>(kAclSmem);
   const int C = (k + W + kAclKeys - 1) / kAclKeys;
   launch_k(k_sparse_attn_cl<NPART>, dim3((unsigned)(C * (H / kAclHeads)), (unsigned)c.batch), dim3(kAclThreads),
            kAclSmem, s, (unsigned)C, q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H,
-           out);
+           out, q_early);
 }
 
 // The key-split form covers 64-head groups and up to 1,024 keys per row; the
@@ -326,12 +326,15 @@ bool attn_key_split(int H, int k, int W) {
   return v == 1 && H % kAclHeads == 0 && k + W >= 1 && k + W <= kAclKeys * kAclMaxBlocks;
 }
 
+// q_early: the kernel before this launch on `s` is this library's Top-k, which does
+// not write q (the decode step's Full and Reindex layers); the queries may then be
+// read before waiting for it.
 void launch_attn(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
-                 int k, const uint16_t* swa, int W, float* out, void* ws, cudaStream_t s) {
+                 int k, const uint16_t* swa, int W, float* out, void* ws, cudaStream_t s, int q_early = 0) {
   (void)ws;
   if (attn_key_split(H, k, W)) {
-    if (dt == CSA2_F32) launch_attn_cl<2>(q, dt, H, scale, c, idx, k, swa, W, out, s);
-    else launch_attn_cl<1>(q, dt, H, scale, c, idx, k, swa, W, out, s);
+    if (dt == CSA2_F32) launch_attn_cl<2>(q, dt, H, scale, c, idx, k, swa, W, out, q_early, s);
+    else launch_attn_cl<1>(q, dt, H, scale, c, idx, k, swa, W, out, q_early, s);
   } else {
     if (dt == CSA2_F32) launch_attn_t<2>(q, dt, H, scale, c, idx, k, swa, W, out, s);
     else launch_attn_t<1>(q, dt, H, scale, c, idx, k, swa, W, out, s);
@@ -540,7 +543,8 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
           cudaSuccess)
         return CSA2_ERR_CUDA;
     }
-    launch_attn(L.q, dtype, H, 1.0f / sqrtf((float)CSA2_LATENT_DIM), *main, last, k, L.swa, L.W, L.out, attn_ws, s);
+    launch_attn(L.q, dtype, H, 1.0f / sqrtf((float)CSA2_LATENT_DIM), *main, last, k, L.swa, L.W, L.out, attn_ws, s,
+                L.mode != CSA2_REUSE ? 1 : 0);
   }
   return launch_status();
 }
