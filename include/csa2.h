@@ -201,7 +201,10 @@ typedef struct {
  *   REUSE: attends with the indices of the latest Full/Reindex layer.
  * The first layer must be FULL. layers is a host array of n_layers descriptors.
  * q, q_idx, q_idx2 share ``dtype``. ws: at least csa2_workspace_size(...).
- * Launches only; no host synchronisation inside.
+ * Launches only; no host synchronisation inside. The step reads a Full or
+ * Reindex layer's q while that layer's Top-k may still run, so q must not
+ * overlap any layer's idx_out or the workspace (inputs and outputs are distinct
+ * buffers anyway).
  */
 CSA2_API csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, int32_t batch,
                              int32_t H, int32_t k, csa2_dtype dtype, void* ws, size_t ws_bytes,
