@@ -30,6 +30,11 @@
  *    288 + 68 bytes per entry, as on the pages. ``cap`` must be a multiple of
  *    128 and every array 16-byte aligned.
  *  - bf16 tensors are passed as raw 16-bit patterns (uint16_t).
+ *  - Environment switches, read once per process (for measurements):
+ *    CSA2_SCAN_KERNEL=tc runs the streaming indexer scan on the tcgen05 form
+ *    instead of the mma.sync form; CSA2_ATTN_KERNEL=chunked runs attention on
+ *    the chunked form for every shape; CSA2_PDL=0 launches kernels without
+ *    programmatic dependent launch. Results are the same either way.
  */
 #ifndef CSA2_H
 #define CSA2_H
