@@ -34,7 +34,8 @@
  *    CSA2_SCAN_KERNEL=tc runs the streaming indexer scan on the tcgen05 form
  *    instead of the mma.sync form; CSA2_ATTN_KERNEL=chunked runs attention on
  *    the chunked form for every shape; CSA2_PDL=0 launches kernels without
- *    programmatic dependent launch. Results are the same either way.
+ *    programmatic dependent launch. The forms agree within the parity
+ *    tolerances (fp32 rounding order differs; packed bytes are identical).
  */
 #ifndef CSA2_H
 #define CSA2_H
