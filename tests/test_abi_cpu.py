@@ -77,6 +77,8 @@ def test_host_validation_rejects_before_any_launch():
                                 1 << 30, None) == A.ERR_UNSUPPORTED
     assert L.sparse_latent_attn(0x100, A.BF16, 64, 0.04, C.byref(cv), 0x200, 512, None, 5, 0x300, 0x400,
                                 1 << 30, None) == A.ERR_ARG
+    # bounded-wait self-test: a limit over one second is refused before any launch
+    assert L.csa2_selftest_wait_timeout(1_000_000_001, None) == A.ERR_ARG
 
 
 def test_decode_step_validation():
