@@ -7,6 +7,9 @@ public API (kv_quant_append to fill the caches, then one prepared DecodeStep).
   3 1M-token ratio-2 layer (8 x 524,288 entries) with a 16,384-candidate pool
   4 decoder group Full/Reindex/Reuse/Reuse (64 x 65,536 entries, 128-token window)
 
+A Reindex layer scores its own indexer-key array (``reindex_keys="own"``, the
+default) or the Full layer's keys with its own query (``reindex_keys="shared"``).
+
 Sizes can be reduced (batch, tokens) for tests; the structure stays the same.
 All inputs come from ``workloads`` (seeded, synthetic).
 """
@@ -26,7 +29,8 @@ CONFIGS = {
     3: dict(name="1M-token ratio-2 layer, hierarchical indexer", B=8, tokens=1048576, ratio=2, H=64,
             dtype=torch.bfloat16, src="lognormal", seed=2, modes=(FULL,), pool=16384, W=0),
     4: dict(name="decoder group Full/Reindex/Reuse/Reuse", B=64, tokens=65536, ratio=1, H=64,
-            dtype=torch.bfloat16, src="lognormal", seed=3, modes=(FULL, REINDEX, REUSE, REUSE), pool=0, W=128),
+            dtype=torch.bfloat16, src="lognormal", seed=3, modes=(FULL, REINDEX, REUSE, REUSE), pool=0, W=128,
+            reindex_keys="own"),
 }
 TOPK = 512
 
@@ -75,7 +79,7 @@ class DecodeWorkload:
         B, H, dt = c["B"], c["H"], c["dtype"]
         self.cache = fill_cache(c, extra)
         self.reindex_keys = None
-        if REINDEX in c["modes"]:
+        if REINDEX in c["modes"] and c.get("reindex_keys", "own") == "own":
             self.reindex_keys = fill_cache(c, extra, stream="reindex-keys")  # only its indexer keys are read
         self.layers, self.inputs = [], []
         for li, mode in enumerate(c["modes"]):
@@ -86,7 +90,8 @@ class DecodeWorkload:
             swa = WL.window(c["seed"], li, B, c["W"], device="cuda") if c["W"] else None
             out = torch.empty(B, H, 512, dtype=torch.float32, device="cuda")
             idx_out = torch.empty(B, TOPK, dtype=torch.int32, device="cuda")
-            own = (self.reindex_keys.idx_codes, self.reindex_keys.idx_scales) if mode == REINDEX else (None, None)
+            own = ((self.reindex_keys.idx_codes, self.reindex_keys.idx_scales)
+                   if mode == REINDEX and self.reindex_keys is not None else (None, None))
             self.layers.append(Layer(mode, q, out, cache=self.cache if mode == FULL else None,
                                      q_idx=None if mode == REUSE else q_idx, w_idx=None if mode == REUSE else w_idx,
                                      own_idx_codes=own[0], own_idx_scales=own[1], pool=c["pool"] if mode == FULL else 0,

@@ -22,8 +22,12 @@ title and section:
           "Tre meccanismi", second and third paragraphs.
 
 The pages give no formula for the indexer score, the attention scale, the
-tie rule or the merge arithmetic; the readings used here are the ones listed in
-DESIGN.md ("Readings of the pages"), and each is restated where it is used.
+tie rule or the merge arithmetic. Each function states the reading it takes
+where the pages are silent: the merge is two rounded float32 products and one
+rounded sum; the score is sum_h w_h * max(0, q_h . k) over 4 indexer heads; ties
+in the Top-k go to the lower position and the output is ascending; attention
+is scaled by 1/sqrt(512) and the window rows join the selected entries in one
+softmax.
 
 Floating point: quantisation decisions are taken in IEEE float32, the precision
 of the quantiser's inputs (numpy float32 arithmetic rounds each operation to

@@ -17,7 +17,7 @@ sections "Cache principal" and "Cles d'indexeur"):
 * E8M0 (the MX block-scale format): 8-bit biased exponent, value 2**(e-127),
   0xFF is NaN.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 * Rounding is round-to-nearest, ties to the code with an even mantissa bit
   (IEEE round-half-even applied to the target grid), saturating to the largest
   finite magnitude ("satfinite").

@@ -119,6 +119,7 @@ def assert_topk_match(got_idx, ref_idx, ref_scores, positions=None, where=""):
     score_of = dict(zip(pos.tolist(), s.tolist()))
     tau = min(score_of[p] for p in vr.tolist())
     for p in diff:
+        assert p in score_of, f"{where}: position {p} is not among the candidates"
         assert abs(score_of[p] - tau) <= TIE_REL * abs(tau), \
             f"{where}: position {p} (score {score_of[p]}) differs, kth score {tau}"
     return len(diff)

@@ -346,3 +346,149 @@ def check_attention(sparse_attention):
                        rtol=1e-12, atol=1e-14)
     perm = rng.permutation(37)
     assert np.allclose(sparse_attention(q, v[perm]), got, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------ window and layer-mode pins
+# Independent decoders of the packed cache bytes: the E2M1 value table of the golden
+# file, torch's float8_e4m3fn cast for the main scales and 2^(e-127) for E8M0; nibbles
+# split with plain integer arithmetic (channel 2j low, 2j+1 high).
+def _nibbles_ref(packed):
+    p = np.asarray(packed, np.int64)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), np.int64)
+    out[..., 0::2] = p % 16
+    out[..., 1::2] = p // 16
+    return out
+
+
+def latents_ref(lat_codes, lat_scales):
+    """[n, 256] packed codes + [n, 32] E4M3 scale bytes -> float64 [n, 512]."""
+    table = np.array(golden("e2m1_e8m0.json")["e2m1_values_by_code"], np.float64)
+    vals = table[_nibbles_ref(lat_codes)]
+    sc = torch.from_numpy(np.ascontiguousarray(lat_scales, np.uint8)).view(torch.float8_e4m3fn)
+    sc = sc.to(torch.float64).numpy()
+    return vals * np.repeat(sc, 16, axis=-1)
+
+
+def keys_ref(idx_codes, idx_scales):
+    """[n, 64] packed codes + [n, 4] E8M0 bytes -> float64 [n, 128]."""
+    table = np.array(golden("e2m1_e8m0.json")["e2m1_values_by_code"], np.float64)
+    vals = table[_nibbles_ref(idx_codes)]
+    sc = np.exp2(np.asarray(idx_scales, np.float64) - golden("e2m1_e8m0.json")["e8m0_bias"])
+    return vals * np.repeat(sc, 32, axis=-1)
+
+
+def sdpa_ref(q, rows):
+    """Dense float64 softmax attention of q [H, 512] over rows [m, 512] with K = V = rows,
+    scale 1/sqrt(512) (torch's library routine)."""
+    t = torch.from_numpy(np.ascontiguousarray(rows, np.float64))[None]
+    return torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(np.ascontiguousarray(q, np.float64))[None], t, t, scale=1 / math.sqrt(512))[0].numpy()
+
+
+def random_cache_rows(rng, n):
+    """Packed rows of n entries: every byte is a valid pair of E2M1 codes; E4M3 scale
+    bytes 0x28..0x4F (about 0.25 to 15), E8M0 bytes 120..134."""
+    return (rng.integers(0, 256, (n, 256), dtype=np.uint8), rng.integers(0x28, 0x50, (n, 32), dtype=np.uint8),
+            rng.integers(0, 256, (n, 64), dtype=np.uint8), rng.integers(120, 135, (n, 4), dtype=np.uint8))
+
+
+def check_attend_window(attend):
+    """Selected entries and window rows share one softmax: attend over k > 0 entries
+    and W > 0 window rows equals dense attention over the concatenation of the
+    dequantised selected rows and the window rows ("Le cache KV en FP4", "La
+    contrepartie : la fenetre glissante"; "890 octets", "Troisiemement")."""
+    rng = np.random.default_rng(21)
+    lc, ls, _, _ = random_cache_rows(rng, 400)
+    lat = latents_ref(lc, ls)
+    for k_sel, W, wscale in [(37, 5, 1.0), (200, 128, 3.0), (1, 1, 0.3), (300, 64, 8.0)]:
+        q = rng.standard_normal((6, 512)) / math.sqrt(512) * 4
+        sel = np.sort(rng.choice(400, k_sel, replace=False))
+        idx = np.concatenate([sel, -np.ones(9, np.int64)])
+        rng.shuffle(idx)
+        win = rng.standard_normal((W, 512)) * wscale
+        got = attend(q, lc, ls, idx, win)
+        ref = sdpa_ref(q, np.concatenate([lat[sel], win]))
+        assert np.allclose(got, ref, rtol=1e-11, atol=1e-12), (k_sel, W)
+        # both halves carry weight: the joint result is neither part alone
+        assert not np.allclose(got, sdpa_ref(q, lat[sel]), rtol=1e-6, atol=1e-9)
+        assert not np.allclose(got, sdpa_ref(q, win), rtol=1e-6, atol=1e-9)
+
+
+class _HostCache:
+    """A plain container with the oracle cache's fields (no oracle code)."""
+
+    def __init__(self, rows_per_seq):
+        B, cap = len(rows_per_seq), max(r[0].shape[0] for r in rows_per_seq) + 8
+        self.batch, self.cap = B, cap
+        self.lat_codes = np.zeros((B, cap, 256), np.uint8)
+        self.lat_scales = np.zeros((B, cap, 32), np.uint8)
+        self.idx_codes = np.zeros((B, cap, 64), np.uint8)
+        self.idx_scales = np.zeros((B, cap, 4), np.uint8)
+        self.len = np.zeros(B, np.int64)
+        for b, (lc, ls, ic, isc) in enumerate(rows_per_seq):
+            n = lc.shape[0]
+            self.lat_codes[b, :n], self.lat_scales[b, :n] = lc, ls
+            self.idx_codes[b, :n], self.idx_scales[b, :n] = ic, isc
+            self.len[b] = n
+
+
+def check_decode_modes(decode_step, FULL, REINDEX, REUSE):
+    """Layer modes ("890 octets de cache KV par token", "Deuxiemement"):
+      * a Reindex layer with its own key array selects the Top-k of its own query
+        scored against THOSE keys and attends over the Full layer's main KV;
+      * after a Full layer that built a hierarchical pool, a Reindex layer (own keys
+        or the shared ones) ranks only the pool's positions;
+      * Reuse attends, with its own query, over the latest Full/Reindex selection.
+    References: brute-force scores (math.fsum) and Top-k (sorted), dense attention
+    by the library routine, keys and latents decoded by the independent decoders."""
+    rng = np.random.default_rng(22)
+    B, n, H, k, P = 2, 300, 4, 8, 40
+    rows = [random_cache_rows(rng, n) for _ in range(B)]
+    own = [random_cache_rows(rng, n) for _ in range(B)]
+    main, own_c = _HostCache(rows), _HostCache(own)
+    q = [rng.standard_normal((B, H, 512)) / math.sqrt(512) * 4 for _ in range(3)]
+    qi = [rng.standard_normal((B, 4, 128)) / math.sqrt(128) for _ in range(3)]
+    wi = [rng.uniform(0, 1, (B, 4)) for _ in range(3)]
+
+    def brute_sel(b, qq, ww, keys, positions):
+        s = scores_brute(qq, ww, keys[positions])
+        return topk_brute(s, k, positions)
+
+    # --- Full -> Reindex (own keys) -> Reuse, no pool
+    layers = [dict(mode=FULL, cache=main, q_idx=qi[0], w_idx=wi[0], q=q[0]),
+              dict(mode=REINDEX, keys_codes=own_c.idx_codes, keys_scales=own_c.idx_scales, q_idx=qi[1],
+                   w_idx=wi[1], q=q[1]),
+              dict(mode=REUSE, q=q[2])]
+    outs, idxs = decode_step(layers, k)
+    for b in range(B):
+        km, ko = keys_ref(rows[b][2], rows[b][3]), keys_ref(own[b][2], own[b][3])
+        lat = latents_ref(rows[b][0], rows[b][1])
+        allpos = list(range(n))
+        e0 = brute_sel(b, qi[0][b], wi[0][b], km, allpos)
+        e1 = brute_sel(b, qi[1][b], wi[1][b], ko, allpos)
+        assert e1 != brute_sel(b, qi[1][b], wi[1][b], km, allpos)  # own keys decide
+        assert list(idxs[0][b]) == e0 and list(idxs[1][b]) == e1 and list(idxs[2][b]) == e1
+        assert np.allclose(outs[0][b], sdpa_ref(q[0][b], lat[e0]), rtol=1e-11, atol=1e-12)
+        assert np.allclose(outs[1][b], sdpa_ref(q[1][b], lat[e1]), rtol=1e-11, atol=1e-12)
+        assert np.allclose(outs[2][b], sdpa_ref(q[2][b], lat[e1]), rtol=1e-11, atol=1e-12)
+
+    # --- Full with a pool -> Reindex (shared keys) -> Reindex (own keys) -> Reuse
+    qp, wp = rng.standard_normal((B, 4, 128)) / math.sqrt(128), rng.uniform(0, 1, (B, 4))
+    layers = [dict(mode=FULL, cache=main, q_idx=qi[0], w_idx=wi[0], pool=P, q_idx2=qp, w_idx2=wp, q=q[0]),
+              dict(mode=REINDEX, q_idx=qi[1], w_idx=wi[1], q=q[1]),
+              dict(mode=REINDEX, keys_codes=own_c.idx_codes, keys_scales=own_c.idx_scales, q_idx=qi[2],
+                   w_idx=wi[2], q=q[2]),
+              dict(mode=REUSE, q=q[1])]
+    outs, idxs = decode_step(layers, k)
+    for b in range(B):
+        km, ko = keys_ref(rows[b][2], rows[b][3]), keys_ref(own[b][2], own[b][3])
+        lat = latents_ref(rows[b][0], rows[b][1])
+        pool = [p for p in topk_brute(scores_brute(qi[0][b], wi[0][b], km), P) if p >= 0]
+        e0 = brute_sel(b, qp[b], wp[b], km, pool)
+        e1 = brute_sel(b, qi[1][b], wi[1][b], km, pool)
+        e2 = brute_sel(b, qi[2][b], wi[2][b], ko, pool)
+        assert e1 != brute_sel(b, qi[1][b], wi[1][b], km, list(range(n)))  # the pool decides
+        assert e2 != brute_sel(b, qi[2][b], wi[2][b], ko, list(range(n)))
+        assert [list(idxs[i][b]) for i in range(4)] == [e0, e1, e2, e2]
+        for i, (qq, sel) in enumerate([(q[0], e0), (q[1], e1), (q[2], e2), (q[1], e2)]):
+            assert np.allclose(outs[i][b], sdpa_ref(qq[b], lat[sel]), rtol=1e-11, atol=1e-12), i

@@ -106,3 +106,47 @@ def test_hsi_rescoring_with_the_wrong_indexer_is_caught():
     def bad(keys, q1, w1, q2, w2, pool=16384, k=512):
         return csa2.hsi_select(keys, q1, w1, q1, w1, pool, k)
     _fails(P.check_hsi, bad, csa2.indexer_scores, csa2.topk_positions)
+
+
+def test_window_as_a_second_softmax_is_caught():
+    def averaged(q, lc, ls, idx, swa=None, scale=None):  # two softmaxes, averaged
+        a = csa2.attend(q, lc, ls, idx, None, scale)
+        return a if swa is None or not len(swa) else 0.5 * (a + csa2.attend(q, lc, ls, -np.ones(1, int), swa, scale))
+    _fails(P.check_attend_window, averaged)
+
+    def summed(q, lc, ls, idx, swa=None, scale=None):  # two softmaxes, summed
+        a = csa2.attend(q, lc, ls, idx, None, scale)
+        return a if swa is None or not len(swa) else a + csa2.attend(q, lc, ls, -np.ones(1, int), swa, scale)
+    _fails(P.check_attend_window, summed)
+
+    _fails(P.check_attend_window, lambda q, lc, ls, idx, swa=None, scale=None: csa2.attend(q, lc, ls, idx))
+
+
+def _modes(fn):
+    P.check_decode_modes(fn, csa2.FULL, csa2.REINDEX, csa2.REUSE)
+
+
+def test_reindex_scoring_the_full_layers_keys_is_caught():
+    def full_keys(layers, k):
+        return csa2.decode_step([{a: v for a, v in L.items() if a not in ("keys_codes", "keys_scales")}
+                                 for L in layers], k)
+    _fails(_modes, full_keys)
+
+
+def test_reindex_ignoring_the_pool_is_caught():
+    def no_pool(layers, k):
+        outs, idxs = csa2.decode_step(layers, k)
+        flat = [dict(L, pool=0) if L["mode"] == csa2.FULL else L for L in layers]
+        outs2, idxs2 = csa2.decode_step(flat, k)  # later layers as if no pool had been built
+        return outs[:1] + outs2[1:], idxs[:1] + idxs2[1:]
+    _fails(_modes, no_pool)
+
+
+def test_reuse_of_the_full_selection_instead_of_the_latest_is_caught():
+    def reuse_full(layers, k):
+        outs, idxs = csa2.decode_step(layers, k)
+        first = [layers[0]] + [dict(mode=csa2.REUSE, q=L["q"], swa=L.get("swa")) for L in layers[1:]]
+        outs2, idxs2 = csa2.decode_step(first, k)
+        return ([o2 if L["mode"] == csa2.REUSE else o for L, o, o2 in zip(layers, outs, outs2)],
+                [i2 if L["mode"] == csa2.REUSE else i for L, i, i2 in zip(layers, idxs, idxs2)])
+    _fails(_modes, reuse_full)

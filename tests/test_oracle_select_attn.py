@@ -79,3 +79,11 @@ def test_modes_reuse_and_reindex():
         s = csa2.indexer_scores(qi[b], wi[b], csa2.entry_keys(c.idx_codes[b, :n], c.idx_scales[b, :n]))
         assert np.array_equal(idxs[0][b], csa2.topk_positions(s, k))
         assert np.allclose(outs[1][b], csa2.attend(q2[b], c.lat_codes[b], c.lat_scales[b], idxs[0][b]))
+
+
+def test_attend_window_is_one_joint_softmax_with_the_entries():
+    P.check_attend_window(csa2.attend)
+
+
+def test_decode_modes_reindex_own_keys_pool_and_reuse():
+    P.check_decode_modes(csa2.decode_step, csa2.FULL, csa2.REINDEX, csa2.REUSE)
