@@ -1,20 +1,36 @@
-"""Benchmark of the CSA2 FP4 decode step on B300.
+"""Benchmark of the CSA2 FP4 compressed-KV path on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl ours|reference]
 
-Default workload (config 2): batched decode on a ratio-1 layer at 128K context,
-32 sequences x 131,072 cached entries, 64 query heads x 512, 4-head indexer,
-Top-512. One step = append the step's new token to every sequence (E2M1/E4M3 +
-MXFP4 packing), score every cached entry with the indexer, select the exact
-Top-512, gather/dequantise the selected entries and attend. Metric: decode
-queries/s (one query = one sequence's step), whole job.
+Workloads (``--config``; the default line is 2):
 
-The cache (1.5 GB) is far larger than L2 (126 MB), so every step reads its
-indexer keys from HBM. Timed steps run as CUDA graphs of 16 steps each; the
-indexer scan of every step is bracketed by CUDA events inside the graph.
+  2 batched decode on a ratio-1 layer at 128K context: 32 sequences x 131,072
+    cached entries, 64 query heads x 512, 4-head indexer, Top-512. One step =
+    append the step's new token to every sequence (E2M1/E4M3 + MXFP4 packing),
+    score every cached entry with the indexer, select the exact Top-512,
+    gather/dequantise the selected entries and attend.
+  3 1M-token ratio-2 layer: 8 sequences x 524,288 entries; the Full layer scans
+    every entry, keeps a 16,384-candidate pool, rescores it with a second
+    indexer and selects the Top-512. Two tokens (one merged entry) are appended
+    every other step, one token per step on average.
+  4 decoder group Full/Reindex/Reuse/Reuse over one ratio-1 cache: 64 sequences x
+    65,536 entries, the Reindex layer with its own indexer keys, a 128-row bf16
+    window per layer. The step's token goes into the cache and into the Reindex
+    layer's key array.
+  1 cache write: 65,536 bf16 tokens merged at ratio 2 into 32,768 entries per
+    step (metric: tokens/s).
 
---impl reference times the CPU oracle (tests' reference implementation) on the
-host cores, one sequence per step, on the same workload and metric.
+Metric: decode queries/s (one query = one sequence's step through the layer
+group), whole job; for workload 1, tokens written per second. The caches are
+far larger than L2 (126 MB), so every step reads its indexer keys from HBM;
+workload 1 rotates over four input sets (4 x 84 MB) so its inputs do not stay
+in L2 either. Timed steps run as CUDA graphs of 16 steps; each graph first
+resets the sequence lengths to the workload's size, so every step scans the
+nominal cache plus the tokens appended in that graph. The timed region covers
+at least one second whatever --steps asks (the line reports the steps timed).
+
+--impl reference times the CPU oracle (the tests' reference implementation) on
+the host cores, one sequence per step, on the same workload and metric.
 Under torchrun every rank runs an independent replica on its own GPU (the path
 shards by sequence; no collective); rank 0 prints the JSON line.
 """
@@ -22,6 +38,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import sys
@@ -34,15 +51,17 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 SCAN_BYTES_PER_ENTRY = 68     # indexer key: 64 B codes + 4 B E8M0 scales
-# DRAM read + write bytes per scanned entry of the streaming scan kernel, from one ncu
-# capture of it on 16 x 131,072 entries (146.70 MB / 2,097,152 entries): the keys read
-# once plus the score writes that reach DRAM during the launch. Traffic grows with the
-# entries scanned, so a launch's traffic is this figure times its entries. Valid for the
-# kernel as captured; it has to be measured again whenever the scan kernel changes.
-SCAN_TRAFFIC_PER_ENTRY = 69.95
 GATHER_BYTES_PER_ENTRY = 288  # latent: 256 B codes + 32 B E4M3 scales
+# DRAM read + write bytes per scanned entry of the streaming scan kernel, from one ncu
+# capture of it on 16 x 131,072 entries: the keys read once plus the score writes that
+# reach DRAM during the launch. Traffic grows with the entries scanned, so a launch's
+# traffic is this figure times its entries. None while the kernel has changed since the
+# capture (the line then reports no traffic).
+SCAN_TRAFFIC_PER_ENTRY = 69.95
 STEPS_PER_GRAPH = 16
-REFERENCE_BUDGET_S = 150.0   # longest timed run of the reference arm (the CPU oracle)
+MIN_TIMED_S = 1.0             # shortest timed region
+REFERENCE_BUDGET_S = 150.0    # longest timed run of the reference arm (the CPU oracle)
+TOPK = 512
 
 
 def parse():
@@ -50,10 +69,10 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=4096)
     p.add_argument("--warmup", type=int, default=32)
-    p.add_argument("--config", type=int, default=2)
+    p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--min-seconds", type=float, default=MIN_TIMED_S)
     return p.parse_args()
 
 
@@ -140,44 +159,19 @@ def peaks():
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
     return 6400.0, "fallback"
 
 
-# ----------------------------------------------------------------------------- CPU oracle timing
-def oracle_query_time(c, b, host_cache_rows, inputs, token):
-    """Time one oracle decode query for sequence b: append the token, score, Top-512, attend."""
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_encode(lat, ikey, ratio, w=None):
+    """oracle encode_entries of a whole sequence, 4,096 entries at a time (set-up of
+    the CPU legs; never timed)."""
     from oracle import csa2 as O
-    lc, ls, ic, isc = host_cache_rows
-    q, q_idx, w = inputs
-    t0 = time.perf_counter()
-    new = O.encode_entries(token[0], token[1], 1)
-    lc2 = np.concatenate([lc, new[0]])
-    ls2 = np.concatenate([ls, new[1]])
-    ic2 = np.concatenate([ic, new[2]])
-    is2 = np.concatenate([isc, new[3]])
-    keys = O.entry_keys(ic2, is2)
-    s = O.indexer_scores(q_idx, w, keys)
-    idx = O.topk_positions(s, 512)
-    O.attend(q, lc2, ls2, idx)
-    return time.perf_counter() - t0
-
-
-def oracle_rows(c, b):
-    from oracle import csa2 as O
-    from fp4_compressed_kv_append_b300 import configs as CF
-    lat, ikey = CF.source_tokens(c, b)
-    lat, ikey = lat.cpu().numpy(), ikey.cpu().numpy()
-    parts = [O.encode_entries(lat[i:i + 8192], ikey[i:i + 8192], 1) for i in range(0, len(lat), 8192)]
+    w = [None] * 4 if w is None else list(w)
+    step = 4096 * ratio
+    parts = [O.encode_entries(lat[i:i + step], ikey[i:i + step], ratio, *w) for i in range(0, len(lat), step)]
     return tuple(np.concatenate([p[j] for p in parts]) for j in range(4))
-
-
-def oracle_inputs(c, b):
-    from fp4_compressed_kv_append_b300 import workloads as WL
-    q, q_idx, w = WL.queries(c["seed"], 0, c["B"], c["H"], dtype=c["dtype"], device="cuda")
-    tok = WL.new_token(c["seed"], 0, c["B"], device="cuda")
-    f = lambda t: t[b].float().cpu().numpy().astype(np.float64)  # noqa: E731
-    return (f(q), f(q_idx), f(w)), (tok[0][b].cpu().numpy(), tok[1][b].cpu().numpy())
 
 
 def blas_threads():
@@ -189,249 +183,563 @@ def blas_threads():
         return os.cpu_count()
 
 
-def cpu_baseline(c, budget_s=20.0):
-    rows = oracle_rows(c, 0)
-    inputs, token = oracle_inputs(c, 0)
+class OracleQuery:
+    """One oracle decode query of sequence 0 of a decode workload: append the step's
+    token(s) to the packed rows, then the layer group (scores in float64, Top-512,
+    hierarchical pool, attention with the window)."""
+
+    def __init__(self, c):
+        from fp4_compressed_kv_append_b300 import configs as CF
+        from fp4_compressed_kv_append_b300 import workloads as WL
+        self.c = c
+        f = lambda t: None if t is None else t[0:1].float().cpu().numpy().astype(np.float64)  # noqa: E731
+        w = [x.cpu().numpy() for x in WL.merge_weights(c["seed"], device="cuda")] if c["ratio"] == 2 else None
+        self.w = w
+        lat, ikey = CF.source_tokens(c, 0)
+        self.rows = oracle_encode(lat.cpu().numpy(), ikey.cpu().numpy(), c["ratio"], w)
+        del lat, ikey
+        self.own = None
+        if 1 in c["modes"] and c.get("reindex_keys", "own") == "own":
+            lat, ikey = CF.source_tokens(c, 0, stream="reindex-keys")
+            self.own = oracle_encode(lat.cpu().numpy(), ikey.cpu().numpy(), c["ratio"], w)
+            del lat, ikey
+        self.layers = []
+        for li, mode in enumerate(c["modes"]):
+            q, q_idx, w_idx = WL.queries(c["seed"], li, c["B"], c["H"], dtype=c["dtype"], device="cuda")
+            L = dict(mode=mode, q=f(q), swa=f(WL.window(c["seed"], li, c["B"], c["W"], device="cuda"))
+                     if c["W"] else None)
+            if mode != 2:
+                L.update(q_idx=f(q_idx), w_idx=f(w_idx))
+            if mode == 0 and c["pool"]:
+                _, q2, w2 = WL.queries(c["seed"], li, c["B"], c["H"], dtype=c["dtype"], device="cuda", tag="q2")
+                L.update(pool=c["pool"], q_idx2=f(q2), w_idx2=f(w2))
+            self.layers.append(L)
+        T = c["ratio"]
+        toks = [WL.new_token(c["seed"], s, c["B"], device="cuda") for s in range(T)]
+        self.tok = (np.concatenate([t[0][0].cpu().numpy() for t in toks]),
+                    np.concatenate([t[1][0].cpu().numpy() for t in toks]))
+
+    def __call__(self):
+        from oracle import csa2 as O
+        t0 = time.perf_counter()
+        new = O.encode_entries(self.tok[0], self.tok[1], self.c["ratio"], *(self.w or [None] * 4))
+        rows = [np.concatenate([r, nr]) for r, nr in zip(self.rows, new)]
+        cache = O.Cache(1, rows[0].shape[0])
+        cache.lat_codes[0], cache.lat_scales[0], cache.idx_codes[0], cache.idx_scales[0] = rows
+        cache.len[0] = rows[0].shape[0]
+        layers = [dict(L) for L in self.layers]
+        layers[0]["cache"] = cache
+        if self.own is not None:
+            own = [np.concatenate([r, nr]) for r, nr in zip(self.own[2:], new[2:])]
+            for L in layers:
+                if L["mode"] == O.REINDEX:
+                    L["keys_codes"], L["keys_scales"] = own[0][None], own[1][None]
+        O.decode_step(layers, TOPK)
+        return time.perf_counter() - t0
+
+
+def oracle_decode_sample(c, n_max, budget_s):
+    q = OracleQuery(c)
+    q()  # warm
     times = []
     t_end = time.perf_counter() + budget_s
-    while time.perf_counter() < t_end and len(times) < 50:
-        times.append(oracle_query_time(c, 0, rows, inputs, token))
-    qps = 1.0 / statistics.median(times)
-    return {"value": qps, "unit": "queries/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"{len(times)} decode queries of sequence 0 ({c['tokens']} cached entries): append + "
-                      f"score + Top-512 + attention, numpy float64, median time per query"}
+    while len(times) < n_max and (not times or time.perf_counter() < t_end):
+        times.append(q())
+    return times, (f"decode queries of sequence 0 ({c['tokens'] // c['ratio']:,} cached entries, "
+                   f"layers {'/'.join(['Full', 'Reindex', 'Reuse'][m] for m in c['modes'])}"
+                   f"{', pool ' + str(c['pool']) if c['pool'] else ''}{', window ' + str(c['W']) if c['W'] else ''}):"
+                   f" append + scores + Top-512 + attention, numpy float64")
 
 
-# ----------------------------------------------------------------------------- main
+def oracle_append_sample(c, n_max, budget_s):
+    """The oracle's cache write of 8,192 tokens (bf16 sources, ratio-2 merge)."""
+    from fp4_compressed_kv_append_b300 import workloads as WL
+    from oracle import csa2 as O
+    lat, ikey = WL.outlier_tokens(c["seed"], 0, 8192, device="cpu")
+    lat, ikey = lat.float().numpy(), ikey.float().numpy()
+    w = [x.numpy() for x in WL.merge_weights(c["seed"], device="cpu")]
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < n_max and (not times or time.perf_counter() < t_end):
+        t0 = time.perf_counter()
+        O.encode_entries(lat, ikey, 2, *w)
+        times.append(time.perf_counter() - t0)
+    return times, "8,192-token cache writes (ratio-2 merge, E2M1/E4M3 + MXFP4 packing), numpy float32"
+
+
+def cpu_baseline(c, budget_s=20.0):
+    if c["id"] == 1:
+        times, sample = oracle_append_sample(c, 50, budget_s)
+        v, unit = 8192 / statistics.median(times), "tokens/s"
+    else:
+        times, sample = oracle_decode_sample(c, 50, budget_s)
+        v, unit = 1.0 / statistics.median(times), "queries/s"
+    return {"value": v, "unit": unit, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{len(times)} {sample}; median time per unit"}
+
+
+# ----------------------------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     from fp4_compressed_kv_append_b300 import configs as CF
     if rank != 0:
         return
     c = CF.config(args.config)
-    rows = oracle_rows(c, 0)
-    inputs, token = oracle_inputs(c, 0)
-    # one step = one oracle decode query of sequence 0 (about 0.3 s on the host cores);
-    # the timed queries stop after REFERENCE_BUDGET_S so that any --steps ends within
-    # a few minutes, and the rate comes from the queries timed
-    for _ in range(min(args.warmup, 2)):
-        oracle_query_time(c, 0, rows, inputs, token)
-    times = []
-    t_start = time.perf_counter()
-    while len(times) < max(1, args.steps) and (not times or time.perf_counter() - t_start < REFERENCE_BUDGET_S):
-        times.append(oracle_query_time(c, 0, rows, inputs, token))
+    # one step = one oracle query of sequence 0 (or one 8,192-token write); the timed
+    # steps stop after REFERENCE_BUDGET_S so that any --steps ends within a few minutes
+    if c["id"] == 1:
+        times, sample = oracle_append_sample(c, max(1, args.steps), REFERENCE_BUDGET_S)
+        units, unit, metric = 8192, "tokens/s", "cache-write tokens/s"
+    else:
+        times, sample = oracle_decode_sample(c, max(1, args.steps), REFERENCE_BUDGET_S)
+        units, unit, metric = 1, "queries/s", "decode queries/s"
     t, n = sum(times), len(times)
-    value = n / t
-    sample = (f"{n} decode queries of sequence 0 timed ({args.steps} steps asked; timing stops after "
-              f"{REFERENCE_BUDGET_S:.0f} s): append + score + Top-512 + attention, numpy float64")
-    line = {"impl": "reference", "metric": "decode queries/s", "value": value, "unit": "queries/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / n,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": c["name"], "sequences_per_step": 1,
-                                            "entries": c["tokens"], "heads": c["H"], "topk": 512},
-            "cpu_baseline": {"value": value, "unit": "queries/s", "cores": blas_threads(), "kind": "oracle",
+    value = units * n / t
+    sample = f"{n} {sample} timed ({args.steps} steps asked; timing stops after {REFERENCE_BUDGET_S:.0f} s)"
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": 1,
+            "steps": n, "warmup": 1, "ms_per_step": 1e3 * t / n, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64" if c["id"] != 1 else "f32", "data": "synthetic",
+            "config": {"workload": c["name"], "sequences_per_step": 1, "entries": c["tokens"] // c["ratio"],
+                       "topk": TOPK},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": blas_threads(), "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local):
-    import fp4_compressed_kv_append_b300 as K
-    from fp4_compressed_kv_append_b300 import configs as CF
-    from fp4_compressed_kv_append_b300 import workloads as WL
-
-    torch.cuda.set_device(local)
-    c = CF.config(args.config)
-    if args.config != 2:
-        raise SystemExit("the bench line is defined on config 2 (batched decode at 128K)")
-    B, H, N0 = c["B"], c["H"], c["tokens"]
-    n_graphs = max(1, -(-args.steps // STEPS_PER_GRAPH))
-    K_steps = n_graphs * STEPS_PER_GRAPH
-    warm_graphs = max(1, -(-args.warmup // STEPS_PER_GRAPH))
-    # appends: device-timed graphs (+ warm-up and eager steps), then the e2e run's eager
-    # warm-up, one untimed and the timed graph replays
-    e2e_graphs = max(1, -(-args.e2e_steps // STEPS_PER_GRAPH))
-    total_appends = (warm_graphs + n_graphs + 4) * STEPS_PER_GRAPH + (e2e_graphs + 2) * STEPS_PER_GRAPH
-    wl = CF.DecodeWorkload(c, extra=total_appends)
-    cache = wl.cache
-    tok_lat, tok_key = WL.new_token(c["seed"], 0, B, device="cuda")
-
-    def step(ev=None):
-        """One decode step: append this step's token to every sequence, then the Full
-        layer (indexer scan, cluster Top-512, gather + attention)."""
-        K.kv_quant_append(tok_lat, tok_key, 1, cache)
-        if ev is not None:
-            K.set_scan_events(ev[0], ev[1])
-        wl.step()
-        if ev is not None:
-            K.set_scan_events(None, None)
-
-    # eager warm-up (sets kernel attributes before any capture), then graphs
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
-          for _ in range(K_steps)]
-    for a, b2 in ev:  # the hook takes raw event handles: create them on the device first
-        a.record()
-        b2.record()
-    torch.cuda.synchronize()
-    graphs = []
-    l0 = K.launch_count()
-    for gi in range(n_graphs + warm_graphs):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for s in range(STEPS_PER_GRAPH):
-                j = (gi - warm_graphs) * STEPS_PER_GRAPH + s
-                step(ev[j] if j >= 0 else None)
-        graphs.append(g)
-    launches_per_step = (K.launch_count() - l0) / ((n_graphs + warm_graphs) * STEPS_PER_GRAPH)
-    torch.cuda.synchronize()
-    len_before = int(cache.len[0])
-    for g in graphs[:warm_graphs]:
-        g.replay()
-    torch.cuda.synchronize()
-    n_start = int(cache.len[0])
-    assert K.sync_status() == 0
-
+# ----------------------------------------------------------------------------- timing helpers
+def timed_graph_replays(graphs, n_replays, world, local):
+    """Replay ``graphs`` cyclically n_replays times between CUDA events, with nvidia-smi
+    sampling the clocks; returns (ms, clocks summary)."""
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
     with sampler:
         t0.record()
-        for g in graphs[warm_graphs:]:
-            g.replay()
+        for i in range(n_replays):
+            graphs[i % len(graphs)].replay()
         t1.record()
         torch.cuda.synchronize()
     barrier(world)
-    ms = t0.elapsed_time(t1)
-    ms = max_over_ranks(ms, world)
+    return max_over_ranks(t0.elapsed_time(t1), world), sampler.summary()
+
+
+def graphs_for(args, ms_per_graph):
+    """Timed graph replays: at least --steps steps and at least --min-seconds."""
+    need_steps = -(-args.steps // STEPS_PER_GRAPH)
+    need_time = math.ceil(args.min_seconds * 1e3 / max(ms_per_graph, 1e-3))
+    return max(1, need_steps, need_time)
+
+
+# ----------------------------------------------------------------------------- decode workloads
+class DecodeBench:
+    """Config 2, 3 or 4 on one GPU: the cache, a prepared step, its appends."""
+
+    def __init__(self, c):
+        import fp4_compressed_kv_append_b300 as K
+        from fp4_compressed_kv_append_b300 import configs as CF
+        from fp4_compressed_kv_append_b300 import workloads as WL
+        self.K, self.c = K, c
+        self.wl = CF.DecodeWorkload(c, extra=STEPS_PER_GRAPH)
+        self.base_len = self.wl.cache.len.clone()
+        self.rk = self.wl.reindex_keys
+        self.base_len_rk = self.rk.len.clone() if self.rk is not None else None
+        B, T = c["B"], c["ratio"]
+        toks = [WL.new_token(c["seed"], s, B, device="cuda") for s in range(T)]
+        self.tok = (torch.cat([t[0] for t in toks], 1).contiguous(), torch.cat([t[1] for t in toks], 1).contiguous())
+        self.mw = WL.merge_weights(c["seed"], device="cuda") if T == 2 else (None,) * 4
+        # streaming scans per step: a Full layer's scan, and a Reindex layer's when no pool
+        self.n_scans = sum(1 for m in c["modes"] if m == CF.FULL) + \
+            (sum(1 for m in c["modes"] if m == CF.REINDEX) if not c["pool"] else 0)
+
+    def appends_at(self, j):
+        """Entries appended by step j of a graph (ratio 2: every other step)."""
+        return 1 if self.c["ratio"] == 1 or j % 2 == 1 else 0
+
+    def append(self, tok, j):
+        if self.appends_at(j):
+            self.K.kv_quant_append(tok[0], tok[1], self.c["ratio"], self.wl.cache, *self.mw)
+            if self.rk is not None:
+                self.K.kv_quant_append(tok[0], tok[1], self.c["ratio"], self.rk, *self.mw)
+
+    def reset_len(self):
+        self.wl.cache.len.copy_(self.base_len)
+        if self.rk is not None:
+            self.rk.len.copy_(self.base_len_rk)
+
+    def entries_at(self, j):
+        """Entries per sequence scanned by step j of a graph (after its append)."""
+        return int(self.base_len[0]) + sum(self.appends_at(i) for i in range(j + 1))
+
+    def step_bytes(self, entries):
+        """Algorithmic bytes of one step: indexer keys scanned (68 B per entry per
+        scan), the pool rescoring (68 B per candidate) and the gathered entries (288 B
+        per selected entry per layer)."""
+        c = self.c
+        layers = len(c["modes"])
+        return c["B"] * (self.n_scans * SCAN_BYTES_PER_ENTRY * entries +
+                         (SCAN_BYTES_PER_ENTRY * c["pool"] * (1 + sum(1 for m in c["modes"] if m == 1))
+                          if c["pool"] else 0) +
+                         GATHER_BYTES_PER_ENTRY * TOPK * layers)
+
+
+def run_decode(args, rank, world, local, c):
+    import fp4_compressed_kv_append_b300 as K
+    db = DecodeBench(c)
+    wl, B = db.wl, c["B"]
+
+    def step(j, pairs=None):
+        db.append(db.tok, j)
+        if pairs:
+            K.set_scan_events(pairs)
+        wl.step()
+        if pairs:
+            K.set_scan_events(None)
+
+    for j in range(3):  # eager warm-up (sets kernel attributes before any capture)
+        step(j)
+    db.reset_len()
+    torch.cuda.synchronize()
+
+    def mk_events(n):
+        ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+              for _ in range(n)]
+        for a, b2 in ev:  # the hook takes raw event handles: create them on the device first
+            a.record()
+            b2.record()
+        return ev
+
+    # G distinct graphs of 16 steps, each starting with a length reset; every scan launch
+    # of every step has its own event pair
+    G = 8
+    ev = [[mk_events(db.n_scans) for _ in range(STEPS_PER_GRAPH)] for _ in range(G)]
+    torch.cuda.synchronize()
+    graphs = []
+    l0 = K.launch_count()
+    for gi in range(G):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            db.reset_len()
+            for j in range(STEPS_PER_GRAPH):
+                step(j, ev[gi][j])
+        graphs.append(g)
+    launches_per_step = (K.launch_count() - l0) / (G * STEPS_PER_GRAPH)
+    for g in graphs * 2:  # warm-up replays
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for g in graphs:
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    n_rep = graphs_for(args, t0.elapsed_time(t1) / G)
+    n_rep = -(-n_rep // G) * G  # whole cycles: the events hold the last cycle of the timed region
+    assert K.sync_status() == 0
+    ms, clocks = timed_graph_replays(graphs, n_rep, world, local)
     st = K.sync_status()
     assert st == 0, f"device status {st}"
-    scan_ms = [a.elapsed_time(b) for a, b in ev]
+    K_steps = n_rep * STEPS_PER_GRAPH
+    # scan kernel: events of the last cycle of G graphs
+    scan_ms = [a.elapsed_time(b) for gi in range(G) for j in range(STEPS_PER_GRAPH) for a, b in ev[gi][j]]
+    scan_bytes = [B * SCAN_BYTES_PER_ENTRY * db.entries_at(j) for gi in range(G) for j in range(STEPS_PER_GRAPH)
+                  for _ in range(db.n_scans)]
     scan_avg_ms = sum(scan_ms) / len(scan_ms)
-    # entries scanned per step: the length after that step's append
-    entries = [n_start + i + 1 for i in range(K_steps)]
-    scan_bytes_avg = B * SCAN_BYTES_PER_ENTRY * sum(entries) / K_steps
+    scan_bytes_avg = sum(scan_bytes) / len(scan_bytes)
     hbm_peak, peak_kind = peaks()
     achieved = scan_bytes_avg / (scan_avg_ms * 1e-3) / 1e9
     value = world * B * K_steps / (ms * 1e-3)
-    step_bytes = B * (SCAN_BYTES_PER_ENTRY * sum(entries) / K_steps + GATHER_BYTES_PER_ENTRY * CF.TOPK)
+    step_bytes = sum(db.step_bytes(db.entries_at(j)) for j in range(STEPS_PER_GRAPH)) / STEPS_PER_GRAPH
+    swa_bytes = B * len(c["modes"]) * c["W"] * 512 * 2
 
-    # ---- end to end through the public API with host buffers
-    e2e = e2e_run(args, K, CF, wl, c, tok_lat, tok_key)
-
+    e2e = decode_e2e(args, db)
+    names = ["Full", "Reindex", "Reuse"]
     line = {
         "metric": "decode queries/s", "value": value, "unit": "queries/s", "n_gpus": world,
-        "steps": K_steps, "warmup": warm_graphs * STEPS_PER_GRAPH, "ms_per_step": ms / K_steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32 accumulate (fp4/fp8 cache, bf16 q)",
+        "steps": K_steps, "steps_requested": args.steps, "warmup": 2 * G * STEPS_PER_GRAPH + 3,
+        "ms_per_step": ms / K_steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 accumulate (fp4/fp8 cache, bf16 q)" if c["dtype"] == torch.bfloat16 else
+                 "fp32 accumulate (fp4/fp8 cache, fp32 q)",
         "data": "synthetic",
-        "config": {"workload": c["name"], "sequences": B, "entries": N0, "heads": H, "indexer_heads": 4,
-                   "topk": CF.TOPK, "q_dtype": "bf16", "latents": "fp32 N(0,1) x LogNormal(0,1) per channel",
-                   "step": "kv_quant_append of 1 token/seq + csa2_decode_step (indexer scan, cluster Top-512, "
-                           "gather + sparse attention)",
-                   "l2": "inputs larger than L2 (1.5 GB cache)", "parallelism": f"replicas x{world}",
-                   "cuda_graphs": f"{STEPS_PER_GRAPH} steps per graph"},
+        "config": {"workload": c["name"], "sequences": B, "entries": c["tokens"] // c["ratio"],
+                   "ratio": c["ratio"], "heads": c["H"], "indexer_heads": 4, "topk": TOPK,
+                   "layers": "/".join(names[m] for m in c["modes"]), "pool": c["pool"], "window": c["W"],
+                   "reindex_keys": c.get("reindex_keys") if 1 in c["modes"] else None,
+                   "q_dtype": str(c["dtype"]).replace("torch.", ""),
+                   "latents": "fp32 N(0,1) x LogNormal(0,1) per channel",
+                   "step": "kv_quant_append of the step's token(s) + csa2_decode_step",
+                   "l2": "inputs larger than L2 (caches of 1.5 GB and more)",
+                   "parallelism": f"replicas x{world}",
+                   "cuda_graphs": f"{STEPS_PER_GRAPH} steps per graph, lengths reset at the start of each graph"},
         "step_algorithmic_bytes": step_bytes,
         "step_hbm_gbs": step_bytes / (ms / K_steps * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "indexer scan", "achieved": achieved, "peak": hbm_peak,
+        "step_roofline_frac": step_bytes / (ms / K_steps * 1e-3) / 1e9 / hbm_peak,
+        "swa_bytes_per_step": swa_bytes,
+        "roofline": {"bound": "hbm", "kernel": "indexer scan (streaming)", "achieved": achieved, "peak": hbm_peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "traffic": SCAN_TRAFFIC_PER_ENTRY * scan_bytes_avg / SCAN_BYTES_PER_ENTRY,
-                     "scan_ms": scan_avg_ms, "bytes_per_launch": scan_bytes_avg},
+                     "traffic": (SCAN_TRAFFIC_PER_ENTRY * scan_bytes_avg / SCAN_BYTES_PER_ENTRY
+                                 if SCAN_TRAFFIC_PER_ENTRY else None),
+                     "scan_ms": scan_avg_ms, "bytes_per_launch": scan_bytes_avg, "launches_per_step": db.n_scans},
         "gpu_launches": int(round(launches_per_step * K_steps)),
-        "clocks": sampler.summary(),
+        "clocks": clocks,
         "e2e": e2e,
     }
+    return line
+
+
+def decode_e2e(args, db):
+    """The step end to end through the public API with pinned host buffers: every
+    step copies its inputs (every layer's queries, indexer queries and weights, the
+    new token) host -> device and reads every layer's attention output device ->
+    host. Three measurements:
+      value: eager -- each step calls kv_quant_append and csa2_decode_step through
+        the binding (host API cost included); copies on their own two streams into
+        and out of two sets of device buffers (a serving loop's double buffering);
+      graph_value: the same sequence captured once into CUDA graphs of 16 steps;
+      copy_only: the same copies with no kernels (what the host link allows)."""
+    K, c, wl = db.K, db.c, db.wl
+    B = c["B"]
+    names = ("q", "q_idx", "w_idx", "q_idx2", "w_idx2")
+    host_in = []  # per layer: {name: pinned host tensor}
+    for inp in wl.inputs:
+        host_in.append({n: inp[n].cpu().pin_memory() for n in names if inp.get(n) is not None})
+    h_tok = [t.cpu().pin_memory() for t in db.tok]
+    slots = []
+    for _ in range(2):
+        d = {"in": [{n: torch.empty_like(t, device="cuda") for n, t in hi.items()} for hi in host_in],
+             "tok": [torch.empty_like(t, device="cuda") for t in h_tok],
+             "out": [torch.empty_like(L.out) for L in wl.layers],
+             "h_out": [torch.empty(L.out.shape, dtype=torch.float32).pin_memory() for L in wl.layers]}
+        layers = []
+        for L, dv, out in zip(wl.layers, d["in"], d["out"]):
+            layers.append(K.Layer(L.mode, dv["q"], out, cache=L.cache, q_idx=dv.get("q_idx"), w_idx=dv.get("w_idx"),
+                                  own_idx_codes=L.own_idx_codes, own_idx_scales=L.own_idx_scales, pool=L.pool,
+                                  q_idx2=dv.get("q_idx2"), w_idx2=dv.get("w_idx2"), swa=L.swa,
+                                  idx_out=torch.empty_like(L.idx_out)))
+        d["step"] = K.DecodeStep(layers, TOPK, ws=wl.step.ws)  # steps run in order: one workspace
+        slots.append(d)
+    h2d = sum(t.numel() * t.element_size() for hi in host_in for t in hi.values()) + \
+        sum(t.numel() * t.element_size() for t in h_tok)
+    d2h = sum(t.numel() * 4 for t in slots[0]["h_out"])
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in slots]
+    ev_comp = [torch.cuda.Event() for _ in slots]
+    ev_out = [torch.cuda.Event() for _ in slots]
+
+    def one(i, kernels=True):
+        j = i % 2
+        d = slots[j]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_comp[j])  # the slot's previous step has consumed its inputs
+            for hi, dv in zip(host_in, d["in"]):
+                for n, t in hi.items():
+                    dv[n].copy_(t, non_blocking=True)
+            for ht, dt in zip(h_tok, d["tok"]):
+                dt.copy_(ht, non_blocking=True)
+            ev_in[j].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev_in[j])
+            if i >= 2:
+                s_comp.wait_event(ev_out[j])  # the slot's previous output has been read out
+            if kernels:
+                if i % STEPS_PER_GRAPH == 0:
+                    db.reset_len()
+                db.append(d["tok"], i % STEPS_PER_GRAPH)
+                d["step"](s_comp)
+            ev_comp[j].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[j])
+            for ho, do in zip(d["h_out"], d["out"]):
+                ho.copy_(do, non_blocking=True)
+            ev_out[j].record(s_out)
+
+    def eager(n):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(n):
+            one(i)
+        torch.cuda.synchronize()
+        return time.perf_counter() - t0
+
+    eager(2 * STEPS_PER_GRAPH)  # warm
+    dt = eager(STEPS_PER_GRAPH)
+    n_eager = max(STEPS_PER_GRAPH, int(math.ceil(args.min_seconds / max(dt / STEPS_PER_GRAPH, 1e-6))))
+    n_eager = -(-n_eager // STEPS_PER_GRAPH) * STEPS_PER_GRAPH
+    dt_eager = eager(n_eager)
+    assert K.sync_status() == 0
+
+    def graph(kernels):
+        cap = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for s in (s_in, s_comp, s_out):
+                s.wait_stream(cap)
+            for i in range(STEPS_PER_GRAPH):
+                one(i, kernels)
+            for s in (s_in, s_comp, s_out):
+                cap.wait_stream(s)
+        g.replay()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        g.replay()
+        torch.cuda.synchronize()
+        per = time.perf_counter() - t0
+        n = max(1, int(math.ceil(args.min_seconds / max(per, 1e-6))))
+        t0 = time.perf_counter()
+        for _ in range(n):
+            g.replay()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / (n * STEPS_PER_GRAPH), n * STEPS_PER_GRAPH
+
+    t_graph, n_graph = graph(True)
+    t_copy, n_copy = graph(False)
+    assert K.sync_status() == 0
+    return {"value": B * n_eager / dt_eager, "unit": "queries/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n_eager,
+            "api": "kv_quant_append + csa2_decode_step called through the binding every step, pinned host "
+                   "buffers, copies double-buffered on their own streams",
+            "graph_value": B / t_graph, "graph_steps": n_graph,
+            "copy_only": {"us_per_step": 1e6 * t_copy, "steps": n_copy,
+                          "h2d_plus_d2h_gbs": (h2d + d2h) / t_copy / 1e9,
+                          "what": "the same copies and stream order captured in graphs, no kernels"}}
+
+
+# ----------------------------------------------------------------------------- cache-write workload
+def run_append(args, rank, world, local, c):
+    """Config 1: one step writes 65,536 bf16 tokens (ratio-2 merge) into a layer's
+    cache; the cache length is reset first, so every step writes the same rows."""
+    import fp4_compressed_kv_append_b300 as K
+    from fp4_compressed_kv_append_b300 import workloads as WL
+    T = c["tokens"]
+    n_sets = 4  # 4 x 84 MB of sources: more than L2 holds, so each step reads its inputs from HBM
+    srcs = [tuple(t[None].contiguous() for t in WL.outlier_tokens(c["seed"], s, T, device="cuda"))
+            for s in range(n_sets)]
+    entries = T // 2
+    cache = K.Cache(1, (entries + 127) // 128 * 128)
+    zero = torch.zeros_like(cache.len)
+    mw = WL.merge_weights(c["seed"], device="cuda")
+    in_bytes = T * (512 + 128) * 2
+    out_bytes = entries * (288 + 68)
+    alg_bytes = in_bytes + out_bytes
+
+    def step(j, ev=None):
+        cache.len.copy_(zero)
+        if ev:
+            ev[0].record()
+        K.kv_quant_append(srcs[j % n_sets][0], srcs[j % n_sets][1], 2, cache, *mw)
+        if ev:
+            ev[1].record()
+
+    for j in range(4):
+        step(j)
+    torch.cuda.synchronize()
+    assert K.sync_status() == 0 and int(cache.len[0]) == entries
+    G = 4
+    ev = [[(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+           for _ in range(STEPS_PER_GRAPH)] for _ in range(G)]
+    for row in ev:  # create the events on the device before the capture
+        for a, b2 in row:
+            a.record()
+            b2.record()
+    torch.cuda.synchronize()
+    graphs = []
+    l0 = K.launch_count()
+    for gi in range(G):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for j in range(STEPS_PER_GRAPH):
+                step(j, ev[gi][j])
+        graphs.append(g)
+    launches_per_step = (K.launch_count() - l0) / (G * STEPS_PER_GRAPH)
+    for g in graphs * 2:
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for g in graphs:
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    n_rep = graphs_for(args, t0.elapsed_time(t1) / G)
+    n_rep = -(-n_rep // G) * G
+    ms, clocks = timed_graph_replays(graphs, n_rep, world, local)
+    assert K.sync_status() == 0
+    K_steps = n_rep * STEPS_PER_GRAPH
+    k_ms = [a.elapsed_time(b) for gi in range(G) for a, b in ev[gi]]
+    k_avg = sum(k_ms) / len(k_ms)
+    hbm_peak, peak_kind = peaks()
+    achieved = alg_bytes / (k_avg * 1e-3) / 1e9
+
+    # e2e: the step's sources copied in from pinned host memory, the new length read back
+    h_src = [tuple(t.cpu().pin_memory() for t in s) for s in srcs[:2]]
+    d_src = [tuple(torch.empty_like(t) for t in s) for s in srcs[:2]]
+    h_len = torch.empty(1, dtype=torch.int32).pin_memory()
+    s_in = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+
+    def one(i):
+        j = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_done[j])
+            for dt_, ht in zip(d_src[j], h_src[j]):
+                dt_.copy_(ht, non_blocking=True)
+            ev_in[j].record(s_in)
+        cur = torch.cuda.current_stream()
+        cur.wait_event(ev_in[j])
+        cache.len.copy_(zero)
+        K.kv_quant_append(d_src[j][0], d_src[j][1], 2, cache, *mw)
+        h_len.copy_(cache.len, non_blocking=True)
+        ev_done[j].record(cur)
+
+    for i in range(4):
+        one(i)
+    torch.cuda.synchronize()
+    t_s = time.perf_counter()
+    i = 0
+    while True:
+        one(i)
+        i += 1
+        if i % 8 == 0:
+            torch.cuda.synchronize()
+            if time.perf_counter() - t_s >= args.min_seconds:
+                break
+    dt = time.perf_counter() - t_s
+    assert K.sync_status() == 0 and int(h_len[0]) == entries
+    e2e = {"value": T * i / dt, "unit": "tokens/s", "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4,
+           "steps": i, "api": "kv_quant_append through the binding every step; sources copied in from pinned "
+                              "host memory on their own stream (double-buffered), the new length read back"}
+    return {
+        "metric": "cache-write tokens/s", "value": world * T * K_steps / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": K_steps, "steps_requested": args.steps, "warmup": 2 * G * STEPS_PER_GRAPH + 4,
+        "ms_per_step": ms / K_steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 arithmetic (bf16 sources, fp4/fp8 codes out)", "data": "synthetic",
+        "config": {"workload": c["name"], "tokens": T, "entries": entries, "ratio": 2,
+                   "sources": "bf16 N(0,1), 1% of channels x20", "input_sets": n_sets,
+                   "l2": f"{n_sets} input sets of {in_bytes / 1e6:.1f} MB rotated (larger than L2)",
+                   "parallelism": f"replicas x{world}",
+                   "cuda_graphs": f"{STEPS_PER_GRAPH} steps per graph, length reset before each step"},
+        "step_algorithmic_bytes": alg_bytes,
+        "roofline": {"bound": "hbm", "kernel": "quant_append (+ length update)", "achieved": achieved,
+                     "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": None, "kernel_ms": k_avg, "bytes_per_launch": alg_bytes},
+        "gpu_launches": int(round(launches_per_step * K_steps)),
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+
+
+def run_ours(args, rank, world, local):
+    from fp4_compressed_kv_append_b300 import configs as CF
+    torch.cuda.set_device(local)
+    c = CF.config(args.config)
+    line = run_append(args, rank, world, local, c) if args.config == 1 else run_decode(args, rank, world, local, c)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(c)
     if rank == 0:
         print(json.dumps(line), flush=True)
-
-
-def e2e_run(args, K, CF, wl, c, tok_lat, tok_key):
-    """The same step through the public API (kv_quant_append + csa2_decode_step) with
-    pinned host buffers: every step copies its inputs (q, q_idx, w, the new token)
-    host -> device and reads its attention output device -> host. The steps run in
-    order on one compute stream (each step's append before its scan); the copies run
-    on their own two streams into and out of two sets of device buffers, so a step's
-    copies overlap the neighbouring steps' kernels (a serving loop's double buffering).
-    """
-    B, H = c["B"], c["H"]
-    L0 = wl.layers[0]
-    h_q = L0.q.cpu().pin_memory()
-    h_qi = L0.q_idx.cpu().pin_memory()
-    h_w = L0.w_idx.cpu().pin_memory()
-    h_tl, h_tk = tok_lat.cpu().pin_memory(), tok_key.cpu().pin_memory()
-    n_slots = 2
-    slots = []
-    for _ in range(n_slots):
-        d = dict(q=torch.empty_like(L0.q), qi=torch.empty_like(L0.q_idx), w=torch.empty_like(L0.w_idx),
-                 tl=torch.empty_like(tok_lat), tk=torch.empty_like(tok_key), out=torch.empty_like(L0.out),
-                 h_out=torch.empty(B, H, 512, dtype=torch.float32).pin_memory())
-        layer = K.Layer(L0.mode, d["q"], d["out"], cache=L0.cache, q_idx=d["qi"], w_idx=d["w"], pool=L0.pool,
-                        idx_out=torch.empty_like(L0.idx_out))
-        d["step"] = K.DecodeStep([layer], CF.TOPK, ws=wl.step.ws)  # steps are in order: one workspace
-        slots.append(d)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_qi, h_w, h_tl, h_tk))
-    d2h = slots[0]["h_out"].numel() * 4
-    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(n_slots)]
-    ev_comp = [torch.cuda.Event() for _ in range(n_slots)]
-    ev_out = [torch.cuda.Event() for _ in range(n_slots)]
-
-    def one(i):
-        j = i % n_slots
-        d = slots[j]
-        with torch.cuda.stream(s_in):
-            if i >= n_slots:
-                s_in.wait_event(ev_comp[j])  # the slot's previous step has consumed its inputs
-            d["q"].copy_(h_q, non_blocking=True)
-            d["qi"].copy_(h_qi, non_blocking=True)
-            d["w"].copy_(h_w, non_blocking=True)
-            d["tl"].copy_(h_tl, non_blocking=True)
-            d["tk"].copy_(h_tk, non_blocking=True)
-            ev_in[j].record(s_in)
-        with torch.cuda.stream(s_comp):
-            s_comp.wait_event(ev_in[j])
-            if i >= n_slots:
-                s_comp.wait_event(ev_out[j])  # the slot's previous output has been read out
-            K.kv_quant_append(d["tl"], d["tk"], 1, wl.cache)
-            d["step"]()
-            ev_comp[j].record(s_comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_comp[j])
-            d["h_out"].copy_(d["out"], non_blocking=True)
-            ev_out[j].record(s_out)
-
-    for i in range(2 * n_slots):  # eager warm-up of the same sequence
-        one(i)
-    torch.cuda.synchronize()
-    # STEPS_PER_GRAPH steps per CUDA graph (copies, appends and steps as captured
-    # nodes on the three streams); replays are serialised on one stream
-    cap = torch.cuda.Stream()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=cap):
-        for s in (s_in, s_comp, s_out):
-            s.wait_stream(cap)
-        for i in range(STEPS_PER_GRAPH):
-            one(i)
-        for s in (s_in, s_comp, s_out):
-            cap.wait_stream(s)
-    n_rep = max(1, -(-args.e2e_steps // STEPS_PER_GRAPH))
-    g.replay()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(n_rep):
-        g.replay()
-    torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    assert K.sync_status() == 0
-    steps = n_rep * STEPS_PER_GRAPH
-    return {"value": B * steps / dt, "unit": "queries/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
-            "api": "kv_quant_append + csa2_decode_step, pinned host buffers, copies double-buffered on "
-                   f"their own streams, {STEPS_PER_GRAPH} steps per CUDA graph",
-            "steps": steps}
 
 
 def main():

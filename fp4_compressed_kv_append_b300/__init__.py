@@ -96,17 +96,12 @@ def topk_select(scores, k: int, n=None, out=None, cand=None, stream=None):
     B, stride = scores.shape
     if out is None:
         out = torch.empty(B, k, dtype=torch.int32, device=scores.device)
-    A.check(A.lib().topk_select(_ptr(scores), _ptr(n), stride, k, _ptr(cand), _ptr(out), B, None, 0,
-                                _stream(stream)), "topk_select")
+    A.check(A.lib().topk_select(_ptr(scores), _ptr(n), stride, k, _ptr(cand), _ptr(out), B, _stream(stream)),
+            "topk_select")
     return out
 
 
-def attn_workspace_size(batch: int, H: int, k: int, W: int = 0) -> int:
-    return A.lib().csa2_attn_workspace_size(batch, H, k, W)
-
-
-def sparse_latent_attn(q, cache: Cache, idx, out=None, swa=None, scale: float = DEFAULT_SCALE, ws=None,
-                       stream=None):
+def sparse_latent_attn(q, cache: Cache, idx, out=None, swa=None, scale: float = DEFAULT_SCALE, stream=None):
     """o [B, H, 512] f32 from q [B, H, 512], selected positions idx [B, k], window swa [B, W, 512] bf16."""
     _contig(q, idx, swa, out)
     B, H, _ = q.shape
@@ -114,11 +109,8 @@ def sparse_latent_attn(q, cache: Cache, idx, out=None, swa=None, scale: float = 
     W = 0 if swa is None else swa.shape[1]
     if out is None:
         out = torch.empty(B, H, LATENT_DIM, dtype=torch.float32, device=q.device)
-    need = attn_workspace_size(B, H, k, W)
-    if ws is None or ws.numel() < need:
-        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     A.check(A.lib().sparse_latent_attn(_ptr(q), _dt(q), H, scale, C.byref(cache.view()), _ptr(idx), k, _ptr(swa),
-                                       W, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "sparse_latent_attn")
+                                       W, _ptr(out), _stream(stream)), "sparse_latent_attn")
     return out
 
 
@@ -182,9 +174,13 @@ def launch_count() -> int:
     return A.lib().csa2_launch_count()
 
 
-def set_scan_events(before=None, after=None) -> None:
-    """Measurement hook: record the torch.cuda.Events ``before``/``after`` around every
-    indexer-scan launch made by later calls from this thread (None, None: off). The
-    events must already exist on the device (record them once first)."""
-    A.lib().csa2_set_scan_events(None if before is None else before.cuda_event,
-                                 None if after is None else after.cuda_event)
+def set_scan_events(pairs=None) -> None:
+    """Measurement hook: ``pairs`` is a list of (before, after) torch.cuda.Events; the
+    i-th streaming indexer-scan launch made by later calls from this thread records
+    pair i mod len(pairs) around itself (None or []: off). The events must already
+    exist on the device (record them once first)."""
+    pairs = list(pairs or [])
+    n = len(pairs)
+    before = (C.c_void_p * max(n, 1))(*[a.cuda_event for a, _ in pairs])
+    after = (C.c_void_p * max(n, 1))(*[b.cuda_event for _, b in pairs])
+    A.check(A.lib().csa2_set_scan_events(before, after, n), "csa2_set_scan_events")

@@ -44,21 +44,18 @@ _PROTOS = {
     "indexer_score": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p,
                                 C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p]),
     "topk_select": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32,
-                              C.c_void_p, C.c_size_t, C.c_void_p]),
+                              C.c_void_p]),
     "sparse_latent_attn": (C.c_int, [C.c_void_p, C.c_int, C.c_int32, C.c_float, C.POINTER(CacheView), C.c_void_p,
-                                     C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_size_t,
-                                     C.c_void_p]),
+                                     C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
     "csa2_decode_step": (C.c_int, [C.POINTER(LayerDesc), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int,
                                    C.c_void_p, C.c_size_t, C.c_void_p]),
     "csa2_decode_step_static": (C.c_int, [C.POINTER(LayerDesc), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int,
                                           C.c_void_p]),
     "csa2_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
-    "csa2_topk_workspace_size": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32]),
-    "csa2_attn_workspace_size": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "csa2_sync_status": (C.c_int, [C.c_void_p]),
     "csa2_status_str": (C.c_char_p, [C.c_int]),
     "csa2_launch_count": (C.c_uint64, []),
-    "csa2_set_scan_events": (None, [C.c_void_p, C.c_void_p]),
+    "csa2_set_scan_events": (C.c_int, [C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int32]),
     "csa2_selftest_wait_timeout": (C.c_int, [C.c_uint64, C.c_void_p]),
 }
 

@@ -51,8 +51,9 @@ constexpr int kAclCoef = kAclRedL + 4 * kAclHeads * 4;    // [64] f32
 constexpr int kAclM = kAclCoef + kAclHeads * 4;           // [64] f32: this block's max per head
 constexpr int kAclL = kAclM + kAclHeads * 4;              // [64] f32: this block's sum per head
 constexpr int kAclKeyOk = kAclL + kAclHeads * 4;          // [128] i32
-constexpr int kAclBar = kAclKeyOk + kAclKeys * 4;         // mbarrier (8 B), tensor-memory base (4 B), abort (4 B)
-constexpr int kAclSmem = kAclBar + 16 + 1024;             // + slack to align the base to 1024 bytes
+constexpr int kAclBar = kAclKeyOk + kAclKeys * 4;         // mbarrier (8 B), tensor-memory base (4 B), abort (4 B),
+                                                          // MMA commits issued (4 B)
+constexpr int kAclSmem = kAclBar + 32 + 1024;             // + slack to align the base to 1024 bytes
 // tensor memory: S^T (128 lanes = keys, columns 0..63 = heads), then O^T (four blocks
 // of 128 dims: lanes = dims, columns 64 mb .. 64 mb + 63 = heads)
 constexpr int kAclTmemCols = 256;
@@ -119,9 +120,11 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
   const uint32_t bar = smem_u32addr(smem + kAclBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kAclBar + 8);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kAclBar + 12);
+  volatile uint32_t* n_commits = reinterpret_cast<volatile uint32_t*>(smem + kAclBar + 16);
   if (tid == 0) {
     mbar_init(bar, 1);
     *abort = 0;
+    *n_commits = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   // q_early (set by the decode step when the kernel before this one is its own Top-k,
@@ -291,7 +294,7 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
       __syncthreads();
       tc_fence_after();
     }
-    if (tid == 0) {
+    if (tid == 0 && !*abort) {  // (after a wait that ran out, nothing more is issued)
       const uint32_t vb = smem_u32addr(vs), qb = smem_u32addr(qs);
 #pragma unroll 4
       for (int ks = 0; ks < 32; ++ks) {  // dims 16 ks .. 16 ks + 15: block ks/4, 32 bytes per step
@@ -300,8 +303,9 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
         tc_mma_f16_ss(tmem, da, db, kAclIDesc, (part > 0 || ks > 0) ? 1u : 0u);
       }
       tc_commit(bar);
+      *n_commits = *n_commits + 1;
     }
-    mbar_wait_bounded(bar, (uint32_t)part, abort);  // the MMAs are done reading Q and V
+    mbar_wait_bounded(bar, (uint32_t)part, abort);  // the MMAs are done reading Q and V (or abort is set)
     tc_fence_after();
   }
 
@@ -366,7 +370,7 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (tid == 0) {
+  if (tid == 0 && !*abort) {
     const uint32_t vb = smem_u32addr(vs), pb = smem_u32addr(smem + kAclP);
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb) {
@@ -378,8 +382,9 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
       }
     }
     tc_commit(bar);
+    *n_commits = *n_commits + 1;
   }
-  mbar_wait_bounded(bar, (uint32_t)(NPART & 1), abort);  // the MMAs are done with P and V
+  mbar_wait_bounded(bar, (uint32_t)(NPART & 1), abort);  // the MMAs are done with P and V (or abort is set)
   tc_fence_after();
   // warp w: dims 128 (w / 4) + 32 (w % 4) + lane, all 64 heads
   float ov[64];
@@ -396,6 +401,16 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
   }
   tc_fence_before();
   __syncthreads();  // every read of tensor memory is done; P and V are free
+  if (*abort) {
+    // a wait ran out (CSA2_ERR_TIMEOUT is recorded): let the last committed MMAs finish
+    // (again with a limit) before the tensor memory is freed; the outputs of this
+    // block are then meaningless, but every barrier below is still reached
+    if (tid == 0 && *n_commits > 0) {
+      volatile int again = 0;
+      mbar_wait_bounded(bar, (*n_commits - 1u) & 1u, &again);
+    }
+    __syncthreads();
+  }
   if (w == 0) {
     tc_fence_after();
     tc_dealloc(tmem, kAclTmemCols);

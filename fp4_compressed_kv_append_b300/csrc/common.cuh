@@ -68,25 +68,6 @@ __device__ __forceinline__ float load_elem(const void* p, int dtype, size_t i) {
                            : bf16_bits_to_float(__ldg(static_cast<const uint16_t*>(p) + i));
 }
 
-// ---------------------------------------------------------------- E2M1 (FP4)
-// Round |v| to the nearest E2M1 magnitude, ties to the even mantissa bit,
-// saturating at 6; the sign bit of v becomes bit 3 (a small negative value
-// encodes as 0x8). Magnitudes by code: 0, 0.5, 1, 1.5, 2, 3, 4, 6. The tie
-// points between neighbours are 0.25, 0.75, 1.25, 1.75, 2.5, 3.5 and 5; a tie
-// goes up exactly when the upper neighbour has an even code.
-__device__ __forceinline__ uint32_t e2m1_encode(float v) {
-  const float a = fabsf(v);
-  uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
-               (a >= 3.5f) + (a > 5.0f);
-  return m | ((__float_as_uint(v) >> 28) & 8u);
-}
-
-// E2M1 magnitude of a 3-bit code (exponent bias 1; exponent 0 is subnormal).
-__device__ __forceinline__ float e2m1_magnitude(uint32_t c3) {
-  const uint32_t e = c3 >> 1, m = c3 & 1u;
-  return e == 0 ? 0.5f * (float)m : __uint_as_float(((e - 1u + 127u) << 23) | (m << 22));
-}
-
 // ---------------------------------------------------------------- E4M3 / E8M0
 // float8_e4m3fn code -> float (finite codes; exponent bias 7, subnormals m/8*2^-6).
 __device__ __forceinline__ float e4m3_decode(uint32_t c) {
@@ -113,6 +94,10 @@ __device__ __forceinline__ uint32_t float_order_key(float s) {
   if (u == 0x80000000u) u = 0;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+
+// Score groups: the streaming indexer scan records the largest score of every
+// kGroupRows consecutive entries of a row, for the Top-k that follows it.
+constexpr int kGroupRows = 64;
 
 // Selection key of slot i with score s: (order(s) << 32) | (2^32-1 - i). Keys are
 // distinct, and a larger key is a higher score, then a lower slot.

@@ -20,8 +20,11 @@ namespace {
 
 std::atomic<uint64_t> g_launches{0};
 
-// Measurement hook (csa2_set_scan_events): events recorded around the indexer scan.
-thread_local cudaEvent_t g_scan_ev_before = nullptr, g_scan_ev_after = nullptr;
+// Measurement hook (csa2_set_scan_events): event pairs recorded around the streaming
+// indexer scans, the i-th launch since the hook was set taking pair i mod n.
+constexpr int kMaxScanEvents = 64;
+thread_local cudaEvent_t g_scan_ev_before[kMaxScanEvents], g_scan_ev_after[kMaxScanEvents];
+thread_local int g_scan_ev_n = 0, g_scan_ev_next = 0;
 
 void record_hook_event(cudaEvent_t ev, cudaStream_t s) {
   if (!ev) return;
@@ -90,21 +93,12 @@ csa2_status check_cache(const csa2_cache_view* c) {
   return CSA2_OK;
 }
 
-// sparse_latent_attn keeps its partial results on chip: it needs no scratch.
-size_t attn_ws_bytes(int batch, int H, int k, int W) {
-  (void)batch;
-  (void)H;
-  (void)k;
-  (void)W;
-  return 0;
-}
-
 // ------------------------------------------------------------ launchers (no validation)
 void launch_append(const void* lat, const void* ikey, csa2_dtype dt, int T, int ratio, const float* w0l,
                    const float* w1l, const float* w0i, const float* w1i, const csa2_cache_view& c,
                    cudaStream_t s) {
   const int n_new = T / ratio;
-  const dim3 grid((n_new + kAppendWarps - 1) / kAppendWarps, c.batch);
+  const dim3 grid((n_new + kAppendBlockEntries - 1) / kAppendBlockEntries, c.batch);
   if (dt == CSA2_F32)
     launch_k(k_quant_append<float>, grid, dim3(kAppendWarps * 32), 0, s, 0u, (const float*)lat,
              (const float*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes, c.lat_scales, c.idx_codes,
@@ -240,9 +234,12 @@ bool scan_uses_tcgen05() {
   return v == 1;
 }
 
-void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
+// gmax (streaming mma.sync form only): [batch][cap / kGroupRows] receives the largest
+// score of every kGroupRows entries, for the Top-k after the scan; nullptr for none.
+// Returns whether the group maxima were written.
+bool launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
                  int64_t cap, const int32_t* len, const int32_t* cand, int P, float* scores, int batch,
-                 cudaStream_t s) {
+                 cudaStream_t s, float* gmax = nullptr) {
   g_launches += 1;
   CUtensorMap m;
   if (!cand && cap % kTmaRows == 0 && make_codes_map(&m, codes, (int64_t)batch * cap)) {
@@ -258,7 +255,9 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
     const int64_t tile_rows = scan_uses_tcgen05() ? kTmaRows : kTmaStageRows;
     t.tiles_per_seq = (cap + tile_rows - 1) / tile_rows;
     t.total_tiles = t.tiles_per_seq * batch;
-    record_hook_event(g_scan_ev_before, s);
+    t.gmax = scan_uses_tcgen05() ? nullptr : gmax;
+    const int ev = g_scan_ev_n > 0 ? g_scan_ev_next++ % g_scan_ev_n : -1;
+    if (ev >= 0) record_hook_event(g_scan_ev_before[ev], s);
     if (scan_uses_tcgen05()) {
       if (dt == CSA2_F32) launch_scan_tc<2>(m, t, s);
       else launch_scan_tc<1>(m, t, s);
@@ -266,8 +265,8 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
       if (dt == CSA2_F32) launch_scan_tma<2>(m, t, s);
       else launch_scan_tma<1>(m, t, s);
     }
-    record_hook_event(g_scan_ev_after, s);
-    return;
+    if (ev >= 0) record_hook_event(g_scan_ev_after[ev], s);
+    return t.gmax != nullptr;
   }
   ScanArgs a;
   a.q_idx = q_idx;
@@ -285,6 +284,7 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
   a.total_tiles = a.tiles_per_seq * batch;
   if (dt == CSA2_F32) launch_scan_gather<2>(a, s);
   else launch_scan_gather<1>(a, s);
+  return false;
 }
 
 void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,
@@ -293,6 +293,22 @@ void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, c
   launch_k(k_topk, dim3(kTopkCluster, batch), dim3(kTopkThreads), kTopkSmem, s, 0u, scores, stride, n, cand, k,
            out);
   g_launches += 1;
+}
+
+// Top-k of full rows whose scan recorded group maxima: one block per row bounded by the
+// maxima when k is small against the row (the bound needs at least k groups), the
+// cluster select otherwise.
+void launch_topk_rows(const float* scores, const int32_t* n, int64_t stride, int k, const float* gmax,
+                      int32_t* out, int batch, cudaStream_t s) {
+  if (gmax && k <= (int)kRxListCap && stride / kGroupRows >= 2 * (int64_t)k &&
+      stride <= (int64_t)kTgMaxGroups * kGroupRows) {
+    ensure_max_smem<k_topk_groups>((int)kTgSmem);
+    launch_k(k_topk_groups, dim3(batch), dim3(kTopkThreads), kTgSmem, s, 0u, scores, stride, n, gmax,
+             stride / kGroupRows, k, out);
+    g_launches += 1;
+    return;
+  }
+  launch_topk(scores, n, stride, k, nullptr, out, batch, s);
 }
 
 template <int NPART>
@@ -330,8 +346,7 @@ bool attn_key_split(int H, int k, int W) {
 // not write q (the decode step's Full and Reindex layers); the queries may then be
 // read before waiting for it.
 void launch_attn(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
-                 int k, const uint16_t* swa, int W, float* out, void* ws, cudaStream_t s, int q_early = 0) {
-  (void)ws;
+                 int k, const uint16_t* swa, int W, float* out, cudaStream_t s, int q_early = 0) {
   if (attn_key_split(H, k, W)) {
     if (dt == CSA2_F32) launch_attn_cl<2>(q, dt, H, scale, c, idx, k, swa, W, out, q_early, s);
     else launch_attn_cl<1>(q, dt, H, scale, c, idx, k, swa, W, out, q_early, s);
@@ -377,6 +392,8 @@ csa2_status kv_quant_append(const void* lat, const void* ikey, csa2_dtype in_dty
   if (in_dtype != CSA2_F32 && in_dtype != CSA2_BF16) return CSA2_ERR_ARG;
   if (T < 0 || (ratio != 1 && ratio != 2)) return CSA2_ERR_ARG;
   if (ratio == 2 && ((T & 1) || !w0_lat || !w1_lat || !w0_idx || !w1_idx)) return CSA2_ERR_ARG;
+  if (ratio == 2 && (!aligned16(w0_lat) || !aligned16(w1_lat) || !aligned16(w0_idx) || !aligned16(w1_idx)))
+    return CSA2_ERR_ALIGN;
   if (T == 0) return CSA2_OK;
   if (!lat || !ikey) return CSA2_ERR_ARG;
   if (!aligned16(lat) || !aligned16(ikey)) return CSA2_ERR_ALIGN;
@@ -397,9 +414,7 @@ csa2_status indexer_score(const void* q_idx, csa2_dtype q_dtype, const float* w,
 }
 
 csa2_status topk_select(const float* scores, const int32_t* n, int64_t stride, int32_t k, const int32_t* cand,
-                        int32_t* out_idx, int32_t batch, void* ws, size_t ws_bytes, csa2_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
+                        int32_t* out_idx, int32_t batch, csa2_stream_t stream) {
   if (!scores || !out_idx) return CSA2_ERR_ARG;
   if (stride <= 0 || stride > INT32_MAX || k < 1 || k > CSA2_MAX_TOPK || batch <= 0) return CSA2_ERR_ARG;
   launch_topk(scores, n, stride, k, cand, out_idx, batch, (cudaStream_t)stream);
@@ -408,7 +423,7 @@ csa2_status topk_select(const float* scores, const int32_t* n, int64_t stride, i
 
 csa2_status sparse_latent_attn(const void* q, csa2_dtype q_dtype, int32_t H, float scale,
                                const csa2_cache_view* cache, const int32_t* idx, int32_t k, const uint16_t* swa,
-                               int32_t W, float* out, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+                               int32_t W, float* out, csa2_stream_t stream) {
   const csa2_status cs = check_cache(cache);
   if (cs != CSA2_OK) return cs;
   if (!q || !out || (q_dtype != CSA2_F32 && q_dtype != CSA2_BF16)) return CSA2_ERR_ARG;
@@ -416,26 +431,13 @@ csa2_status sparse_latent_attn(const void* q, csa2_dtype q_dtype, int32_t H, flo
   if (!(scale > 0.f) || k < 0 || k > CSA2_MAX_TOPK || W < 0 || W > CSA2_MAX_WINDOW) return CSA2_ERR_ARG;
   if ((k > 0 && !idx) || (W > 0 && !swa)) return CSA2_ERR_ARG;
   if (!aligned16(q) || !aligned16(out) || (W > 0 && !aligned16(swa))) return CSA2_ERR_ALIGN;
-  (void)ws;
-  (void)ws_bytes;
-  launch_attn(q, q_dtype, H, scale, *cache, idx, k, swa, W, out, ws, (cudaStream_t)stream);
+  launch_attn(q, q_dtype, H, scale, *cache, idx, k, swa, W, out, (cudaStream_t)stream);
   return launch_status();
-}
-
-size_t csa2_attn_workspace_size(int32_t batch, int32_t H, int32_t k, int32_t W) {
-  return attn_ws_bytes(batch, H, k, W);
-}
-
-size_t csa2_topk_workspace_size(int32_t batch, int64_t stride, int32_t k) {
-  (void)batch;
-  (void)stride;
-  (void)k;
-  return 0;
 }
 
 namespace {
 struct StepLayout {
-  size_t scores, pool, pscores, sel, attn, total;
+  size_t scores, gmax, pool, pscores, sel, total;
 };
 
 StepLayout step_layout(int32_t batch, int64_t max_entries, int32_t H, int32_t k, int32_t pool, int32_t W) {
@@ -443,15 +445,17 @@ StepLayout step_layout(int32_t batch, int64_t max_entries, int32_t H, int32_t k,
   size_t off = 0;
   L.scores = off;
   off += round_up((size_t)batch * (size_t)max_entries * sizeof(float), 256);
+  L.gmax = off;
+  off += round_up((size_t)batch * (size_t)(max_entries / kGroupRows + 1) * sizeof(float), 256);
   L.pool = off;
   off += round_up((size_t)batch * (size_t)pool * sizeof(int32_t), 256);
   L.pscores = off;
   off += round_up((size_t)batch * (size_t)pool * sizeof(float), 256);
   L.sel = off;
   off += round_up((size_t)batch * (size_t)k * sizeof(int32_t), 256);
-  L.attn = off;
-  off += attn_ws_bytes(batch, H, k, W);
   L.total = off;
+  (void)H;
+  (void)W;
   return L;
 }
 }  // namespace
@@ -499,13 +503,14 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
   int32_t* pool_idx = reinterpret_cast<int32_t*>(base + SL.pool);
   float* pscores = reinterpret_cast<float*>(base + SL.pscores);
   int32_t* sel = reinterpret_cast<int32_t*>(base + SL.sel);
-  void* attn_ws = base + SL.attn;
+  float* gmax = reinterpret_cast<float*>(base + SL.gmax);
   cudaStream_t s = (cudaStream_t)stream;
   // Top-k of every entry of a cache: scores, then the cluster select
+  // (the scan records the group maxima that bound the Top-k after it)
   auto scan_and_select = [&](const void* qi, const float* wi, const uint8_t* kc, const uint8_t* ksc,
                              const csa2_cache_view* c, int32_t* out_idx) {
-    launch_scan(qi, dtype, wi, kc, ksc, c->cap, c->len, nullptr, 0, scores, batch, s);
-    launch_topk(scores, c->len, c->cap, k, nullptr, out_idx, batch, s);
+    const bool g = launch_scan(qi, dtype, wi, kc, ksc, c->cap, c->len, nullptr, 0, scores, batch, s, gmax);
+    launch_topk_rows(scores, c->len, c->cap, k, g ? gmax : nullptr, out_idx, batch, s);
   };
 
   const csa2_cache_view* main = nullptr;
@@ -518,9 +523,9 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
       main = L.cache;
       pool = L.pool;
       if (pool > 0) {
-        launch_scan(L.q_idx, dtype, L.w_idx, main->idx_codes, main->idx_scales, main->cap, main->len, nullptr, 0,
-                    scores, batch, s);
-        launch_topk(scores, main->len, main->cap, pool, nullptr, pool_idx, batch, s);
+        const bool g = launch_scan(L.q_idx, dtype, L.w_idx, main->idx_codes, main->idx_scales, main->cap,
+                                   main->len, nullptr, 0, scores, batch, s, gmax);
+        launch_topk_rows(scores, main->len, main->cap, pool, g ? gmax : nullptr, pool_idx, batch, s);
         launch_scan(L.q_idx2, dtype, L.w_idx2, main->idx_codes, main->idx_scales, main->cap, main->len, pool_idx,
                     pool, pscores, batch, s);
         launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s);
@@ -543,7 +548,7 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
           cudaSuccess)
         return CSA2_ERR_CUDA;
     }
-    launch_attn(L.q, dtype, H, 1.0f / sqrtf((float)CSA2_LATENT_DIM), *main, last, k, L.swa, L.W, L.out, attn_ws, s,
+    launch_attn(L.q, dtype, H, 1.0f / sqrtf((float)CSA2_LATENT_DIM), *main, last, k, L.swa, L.W, L.out, s,
                 L.mode != CSA2_REUSE ? 1 : 0);
   }
   return launch_status();
@@ -576,9 +581,17 @@ const char* csa2_status_str(csa2_status st) {
 
 uint64_t csa2_launch_count(void) { return g_launches.load(); }
 
-void csa2_set_scan_events(void* before, void* after) {
-  g_scan_ev_before = static_cast<cudaEvent_t>(before);
-  g_scan_ev_after = static_cast<cudaEvent_t>(after);
+csa2_status csa2_set_scan_events(void* const* before, void* const* after, int32_t n) {
+  if (n < 0 || n > kMaxScanEvents || (n > 0 && (!before || !after))) return CSA2_ERR_ARG;
+  for (int i = 0; i < n; ++i)
+    if (!before[i] || !after[i]) return CSA2_ERR_ARG;
+  for (int i = 0; i < n; ++i) {
+    g_scan_ev_before[i] = static_cast<cudaEvent_t>(before[i]);
+    g_scan_ev_after[i] = static_cast<cudaEvent_t>(after[i]);
+  }
+  g_scan_ev_n = n;
+  g_scan_ev_next = 0;
+  return CSA2_OK;
 }
 
 // ---------------------------------------------------------------- allocation-free decode step

@@ -19,7 +19,7 @@ import json
 
 import torch
 
-from . import Cache, DecodeStep, Layer, FULL, attn_workspace_size, indexer_score, kv_quant_append, \
+from . import Cache, DecodeStep, Layer, FULL, indexer_score, kv_quant_append, \
     sparse_latent_attn, topk_select
 from . import workloads as WL
 
@@ -79,7 +79,6 @@ def main():
     scores = torch.empty(B, cache.cap, dtype=torch.float32, device="cuda")
     sel = torch.empty(B, k, dtype=torch.int32, device="cuda")
     out = torch.empty(B, H, 512, dtype=torch.float32, device="cuda")
-    ws = torch.empty(attn_workspace_size(B, H, k, 0), dtype=torch.uint8, device="cuda")
     indexer_score(q_idx, w, cache.idx_codes, cache.idx_scales, cache.len, scores=scores)
     topk_select(scores, k, n=cache.len, out=sel)
     tok = WL.new_token(0, 0, B, device="cuda")
@@ -87,7 +86,7 @@ def main():
         "scan": (lambda: indexer_score(q_idx, w, cache.idx_codes, cache.idx_scales, cache.len, scores=scores),
                  68 * B * N),
         "topk": (lambda: topk_select(scores, k, n=cache.len, out=sel), 4 * B * N),
-        "attn": (lambda: sparse_latent_attn(q, cache, sel, out=out, ws=ws), 288 * B * k),
+        "attn": (lambda: sparse_latent_attn(q, cache, sel, out=out), 288 * B * k),
     }
     if a.kernel in ("append", "all"):
         cache.len.fill_(N - 1)  # the appended token rewrites the last row each launch

@@ -102,7 +102,7 @@ typedef struct {
  *   ratio 1: each token becomes an entry. ratio 2: entry i merges tokens 2i and
  *     2i+1 as e = w0*x_{2i} + w1*x_{2i+1} per channel in float32 (two rounded
  *     products, one rounded sum); T must be even. w0_lat/w1_lat [512] and
- *     w0_idx/w1_idx [128] f32, ignored (may be NULL) for ratio 1.
+ *     w0_idx/w1_idx [128] f32, 16-byte aligned, ignored (may be NULL) for ratio 1.
  *   Latent: per 16 channels s = E4M3(amax/6) (nearest-even, saturating at 448),
  *     code = E2M1(x/s) (float32 division, nearest-even, saturating at 6); s = 0
  *     gives all-zero codes. Indexer key: per 32 channels X = floor(log2 amax)-2
@@ -146,11 +146,10 @@ CSA2_API csa2_status indexer_score(const void* q_idx, csa2_dtype q_dtype, const 
  *   cand == NULL: candidate i is position i. cand != NULL: [batch][stride]
  *     positions (ascending; -1 = empty slot, skipped).
  *   out_idx [batch][k] i32. 1 <= k <= CSA2_MAX_TOPK.
- *   ws/ws_bytes: scratch, at least csa2_topk_workspace_size(batch, stride, k).
+ *   The selection keeps its state in shared memory: no scratch.
  */
 CSA2_API csa2_status topk_select(const float* scores, const int32_t* n, int64_t stride, int32_t k,
-                        const int32_t* cand, int32_t* out_idx, int32_t batch, void* ws,
-                        size_t ws_bytes, csa2_stream_t stream);
+                        const int32_t* cand, int32_t* out_idx, int32_t batch, csa2_stream_t stream);
 
 /*
  * sparse_latent_attn -- gather the selected entries, dequantise, attend.
@@ -165,13 +164,12 @@ CSA2_API csa2_status topk_select(const float* scores, const int32_t* n, int64_t 
  *   swa [batch][W][512] bf16 window rows ("La contrepartie : la fenetre
  *     glissante"; "Troisiemement": 128 tokens), NULL with W = 0.
  *   out [batch][H][512] f32. With no key at all the output row is zero.
- *   ws/ws_bytes: scratch; csa2_attn_workspace_size() is 0 for every shape (the
- *     partial results stay on chip), so ws may be NULL.
+ *   The partial results of a row stay on chip: no scratch.
  */
 CSA2_API csa2_status sparse_latent_attn(const void* q, csa2_dtype q_dtype, int32_t H, float scale,
                                const csa2_cache_view* cache /* host struct */,
                                const int32_t* idx, int32_t k, const uint16_t* swa, int32_t W,
-                               float* out, void* ws, size_t ws_bytes, csa2_stream_t stream);
+                               float* out, csa2_stream_t stream);
 
 /* One layer of a decode step (host struct holding device pointers). */
 typedef struct {
@@ -206,7 +204,8 @@ typedef struct {
  *     Top-k; attends over the main KV of the latest Full layer.
  *   REUSE: attends with the indices of the latest Full/Reindex layer.
  * The first layer must be FULL. layers is a host array of n_layers descriptors.
- * q, q_idx, q_idx2 share ``dtype``. ws: at least csa2_workspace_size(...).
+ * q, q_idx, q_idx2 share ``dtype``. ws: at least csa2_workspace_size(...) bytes,
+ * caller-owned, any contents (every part is written before it is read).
  * Launches only; no host synchronisation inside. The step reads a Full or
  * Reindex layer's q while that layer's Top-k may still run, so q must not
  * overlap any layer's idx_out or the workspace (inputs and outputs are distinct
@@ -243,13 +242,11 @@ CSA2_API csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_l
 CSA2_API csa2_status csa2_decode_step_static(const csa2_layer_desc* layers, int32_t n_layers, int32_t batch,
                                              int32_t H, int32_t k, csa2_dtype dtype, csa2_stream_t stream);
 
-/* Scratch bytes of csa2_decode_step for these sizes (max_entries = cap). */
+/* Scratch bytes of csa2_decode_step for these sizes (max_entries = cap): scores
+ * [batch][max_entries] f32, the largest score of every 64 entries [batch][max_entries
+ * / 64 + 1] f32, pool positions and scores [batch][pool], selection [batch][k]. */
 CSA2_API size_t csa2_workspace_size(int32_t batch, int64_t max_entries, int32_t H, int32_t k, int32_t pool,
                            int32_t W);
-/* Scratch bytes of topk_select / sparse_latent_attn (both 0: they keep their state
- * in shared memory; the arguments are kept for callers that size buffers). */
-CSA2_API size_t csa2_topk_workspace_size(int32_t batch, int64_t stride, int32_t k);
-CSA2_API size_t csa2_attn_workspace_size(int32_t batch, int32_t H, int32_t k, int32_t W);
 
 /* Synchronise ``stream``, return and clear the device status word
  * (CSA2_OK, CSA2_ERR_BOUNDS, CSA2_ERR_TIMEOUT), or CSA2_ERR_CUDA. */
@@ -264,15 +261,16 @@ CSA2_API uint64_t csa2_launch_count(void);
 /*
  * csa2_set_scan_events -- measurement hook for the dominant kernel.
  *
- * Not an operation of the method: lets a benchmark time the indexer scan inside
- * indexer_score and csa2_decode_step. ``before``/``after`` are cudaEvent_t
- * handles (NULL, NULL turns the hook off) that later calls made from this host
- * thread record on their stream right before and right after each streaming
- * indexer-scan launch (as external event nodes while the stream is being
- * captured into a CUDA graph). The caller owns the events and keeps them alive
- * while the hook is set.
+ * Not an operation of the method: lets a benchmark time the streaming indexer
+ * scans inside indexer_score and csa2_decode_step. ``before``/``after`` are host
+ * arrays of n cudaEvent_t handles (0 <= n <= 64; n = 0 turns the hook off). Later
+ * calls made from this host thread record, around the i-th streaming scan launch
+ * since the hook was set, before[i mod n] right before it and after[i mod n] right
+ * after it, on the launch's stream (as external event nodes while the stream is
+ * being captured into a CUDA graph). The caller owns the events and keeps them
+ * alive while the hook is set. CSA2_ERR_ARG for n out of range or a NULL handle.
  */
-CSA2_API void csa2_set_scan_events(void* before, void* after);
+CSA2_API csa2_status csa2_set_scan_events(void* const* before, void* const* after, int32_t n);
 
 /*
  * csa2_selftest_wait_timeout -- test hook for the failure detection.

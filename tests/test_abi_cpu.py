@@ -37,15 +37,11 @@ def test_status_strings():
 
 def test_workspace_sizes():
     L = A.lib()
-    # attention and Top-k keep their state on chip
-    assert L.csa2_attn_workspace_size(32, 64, 512, 0) == 0
-    assert L.csa2_attn_workspace_size(1, 16, 512, 128) == 0
-    assert L.csa2_topk_workspace_size(32, 131072, 512) == 0
-    # the decode step needs the scores, the pool and the selection
+    # the decode step needs the scores, the group maxima, the pool and the selection
     total = L.csa2_workspace_size(32, 131072, 64, 512, 0, 0)
-    assert total >= 32 * 131072 * 4 + 32 * 512 * 4
+    assert total >= 32 * 131072 * 4 + 32 * 2048 * 4 + 32 * 512 * 4
     pooled = L.csa2_workspace_size(8, 524288, 64, 512, 16384, 0)
-    assert pooled >= 8 * 524288 * 4 + 2 * 8 * 16384 * 4 + 8 * 512 * 4
+    assert pooled >= 8 * 524288 * 4 + 8 * 8192 * 4 + 2 * 8 * 16384 * 4 + 8 * 512 * 4
 
 
 def _fake_cache(cap=256, batch=2, base=0x10000):
@@ -70,13 +66,13 @@ def test_host_validation_rejects_before_any_launch():
     assert L.indexer_score(0x100, A.BF16, 0x200, 0x1000, 0x2000, 256, 0x300, 0x400, 20000, 0x500, 2,
                            None) == A.ERR_ARG
     # top-k: k out of range
-    assert L.topk_select(0x100, None, 1000, 0, None, 0x200, 1, None, 0, None) == A.ERR_ARG
-    assert L.topk_select(0x100, None, 1000, 16385, None, 0x200, 1, None, 0, None) == A.ERR_ARG
-    # attention: head count, workspace
-    assert L.sparse_latent_attn(0x100, A.BF16, 48, 0.04, C.byref(cv), 0x200, 512, None, 0, 0x300, 0x400,
-                                1 << 30, None) == A.ERR_UNSUPPORTED
-    assert L.sparse_latent_attn(0x100, A.BF16, 64, 0.04, C.byref(cv), 0x200, 512, None, 5, 0x300, 0x400,
-                                1 << 30, None) == A.ERR_ARG
+    assert L.topk_select(0x100, None, 1000, 0, None, 0x200, 1, None) == A.ERR_ARG
+    assert L.topk_select(0x100, None, 1000, 16385, None, 0x200, 1, None) == A.ERR_ARG
+    # attention: head count, a window without rows
+    assert L.sparse_latent_attn(0x100, A.BF16, 48, 0.04, C.byref(cv), 0x200, 512, None, 0, 0x300,
+                                None) == A.ERR_UNSUPPORTED
+    assert L.sparse_latent_attn(0x100, A.BF16, 64, 0.04, C.byref(cv), 0x200, 512, None, 5, 0x300,
+                                None) == A.ERR_ARG
     # bounded-wait self-test: a limit over one second is refused before any launch
     assert L.csa2_selftest_wait_timeout(1_000_000_001, None) == A.ERR_ARG
 

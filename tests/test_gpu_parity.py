@@ -77,6 +77,51 @@ def test_append_in_two_calls_and_edge_values():
         Hh.assert_rows_equal(cache, b, O.encode_entries(lat[b], key[b], 1))
 
 
+def _tie_rows(n_rows, rng):
+    """Latent rows whose 16-channel blocks have amax = 6 s for an E4M3 scale s, so
+    x / s lands exactly on every E2M1 tie point (0.25, 0.75, ..., 5), on the float32
+    neighbours of the products t s, and on the grid; key rows whose 32-channel blocks
+    have amax = 6 * 2^X, so x * 2^-X does the same for the MXFP4 codes."""
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, 0.0],
+                    np.float32)
+    lat = np.zeros((n_rows, 512), np.float32)
+    key = np.zeros((n_rows, 128), np.float32)
+    for r in range(n_rows):
+        for blk in range(32):
+            e, m = int(rng.integers(-6, 7)), int(rng.integers(0, 8))
+            sc = np.float32((1 + m / 8) * 2.0 ** e)
+            v = (ties[rng.permutation(15)] * sc).astype(np.float32)
+            way = rng.integers(0, 3, 15)  # exact product, next float up, next float down
+            v = np.where(way == 1, np.nextafter(v, np.float32(np.inf)), v)
+            v = np.where(way == 2, np.nextafter(v, np.float32(0)), v).astype(np.float32)
+            v *= np.where(rng.integers(0, 2, 15) == 1, np.float32(-1), np.float32(1))
+            lat[r, 16 * blk:16 * blk + 16] = np.concatenate([[np.float32(6) * sc], v])
+        for blk in range(4):
+            X = int(rng.integers(-20, 20))
+            v = (np.concatenate([ties, ties[:15], [0.1, 0.2]]).astype(np.float32)[rng.permutation(32)] *
+                 np.float32(2.0 ** X)).astype(np.float32)
+            way = rng.integers(0, 3, 32)
+            v = np.where(way == 1, np.nextafter(v, np.float32(np.inf)), v)
+            v = np.where(way == 2, np.nextafter(v, np.float32(0)), v).astype(np.float32)
+            v *= np.where(rng.integers(0, 2, 32) == 1, np.float32(-1), np.float32(1))
+            v[0] = np.float32(6 * 2.0 ** X)
+            key[r, 32 * blk:32 * blk + 32] = v
+    return lat, key
+
+
+def test_append_every_e2m1_tie_point_bit_exact():
+    """The packing rounds x / s (and x * 2^-X) onto E2M1 with ties to the even code,
+    saturating, keeping the sign of zero: every tie point, its float32 neighbours and
+    the grid, with E4M3 scales of every mantissa, against the oracle."""
+    rng = np.random.default_rng(11)
+    lat, key = _tie_rows(96, rng)
+    cache = K.Cache(1, 128)
+    K.kv_quant_append(torch.from_numpy(lat)[None].cuda(), torch.from_numpy(key)[None].cuda(), 1, cache)
+    torch.cuda.synchronize()
+    Hh.assert_rows_equal(cache, 0, O.encode_entries(lat, key, 1))
+    assert K.sync_status() == 0
+
+
 def test_append_past_capacity_is_refused_on_device():
     cache = K.Cache(1, 128)
     lat, ikey = WL.lognormal_tokens(0, 0, 100, device="cuda")
