@@ -19,6 +19,9 @@ Workloads (``--config``; the default line is 2):
     layer's key array.
   1 cache write: 65,536 bf16 tokens merged at ratio 2 into 32,768 entries per
     step (metric: tokens/s).
+  5 prefill store: 1,048,576 bf16 tokens into the four source layers of the
+    global cache (2, 8 and 14 at ratio 2, 20 at ratio 1: 890 bytes per token,
+    0.87 GiB) with one csa2_store_append per step (metric: tokens/s).
 
 Metric: decode queries/s (one query = one sequence's step through the layer
 group), whole job; for workload 1, tokens written per second. The caches are
@@ -69,7 +72,7 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=4096)
     p.add_argument("--warmup", type=int, default=32)
-    p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4])
+    p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--min-seconds", type=float, default=MIN_TIMED_S)
@@ -267,8 +270,30 @@ def oracle_append_sample(c, n_max, budget_s):
     return times, "8,192-token cache writes (ratio-2 merge, E2M1/E4M3 + MXFP4 packing), numpy float32"
 
 
+def oracle_store_sample(c, n_max, budget_s):
+    """The oracle's four-layer store of 4,096 tokens (bf16 sources, ratios 2, 2, 2, 1)."""
+    from fp4_compressed_kv_append_b300 import workloads as WL
+    from oracle import csa2 as O
+    src, w = [], []
+    for layer, ratio in c["layers"]:
+        lat, ikey = WL.outlier_tokens(c["seed"], layer, 4096, device="cpu")
+        src.append((lat.float().numpy(), ikey.float().numpy()))
+        w.append([x.numpy() for x in WL.merge_weights(c["seed"], device="cpu", layer=layer)] if ratio == 2 else None)
+    layers = [(layer, "", ratio) for layer, ratio in c["layers"]]
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < n_max and (not times or time.perf_counter() < t_end):
+        t0 = time.perf_counter()
+        O.store_entries(src, layers, w)
+        times.append(time.perf_counter() - t0)
+    return times, "4,096-token writes into the four source layers (ratios 2, 2, 2, 1), numpy float32"
+
+
 def cpu_baseline(c, budget_s=20.0):
-    if c["id"] == 1:
+    if c["id"] == 5:
+        times, sample = oracle_store_sample(c, 50, budget_s)
+        v, unit = 4096 / statistics.median(times), "tokens/s"
+    elif c["id"] == 1:
         times, sample = oracle_append_sample(c, 50, budget_s)
         v, unit = 8192 / statistics.median(times), "tokens/s"
     else:
@@ -286,7 +311,10 @@ def run_reference(args, rank, world):
     c = CF.config(args.config)
     # one step = one oracle query of sequence 0 (or one 8,192-token write); the timed
     # steps stop after REFERENCE_BUDGET_S so that any --steps ends within a few minutes
-    if c["id"] == 1:
+    if c["id"] == 5:
+        times, sample = oracle_store_sample(c, max(1, args.steps), REFERENCE_BUDGET_S)
+        units, unit, metric = 4096, "tokens/s", "prefill store tokens/s"
+    elif c["id"] == 1:
         times, sample = oracle_append_sample(c, max(1, args.steps), REFERENCE_BUDGET_S)
         units, unit, metric = 8192, "tokens/s", "cache-write tokens/s"
     else:
@@ -297,9 +325,9 @@ def run_reference(args, rank, world):
     sample = f"{n} {sample} timed ({args.steps} steps asked; timing stops after {REFERENCE_BUDGET_S:.0f} s)"
     line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": 1,
             "steps": n, "warmup": 1, "ms_per_step": 1e3 * t / n, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64" if c["id"] != 1 else "f32", "data": "synthetic",
-            "config": {"workload": c["name"], "sequences_per_step": 1, "entries": c["tokens"] // c["ratio"],
-                       "topk": TOPK},
+            "vs_baseline": None, "dtype": "f64" if c["id"] not in (1, 5) else "f32", "data": "synthetic",
+            "config": {"workload": c["name"], "sequences_per_step": 1,
+                       "entries": c["tokens"] // c.get("ratio", 1), "topk": TOPK},
             "cpu_baseline": {"value": value, "unit": unit, "cores": blas_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -731,11 +759,110 @@ def run_append(args, rank, world, local, c):
     }
 
 
+def run_store(args, rank, world, local, c):
+    """Config 5: one step writes 1,048,576 bf16 tokens into the four source layers with
+    one csa2_store_append; the layers' lengths are reset first, so every step writes the
+    same rows. The 5.4 GB of sources are far larger than L2."""
+    import fp4_compressed_kv_append_b300 as K
+    from fp4_compressed_kv_append_b300 import configs as CF
+    st = CF.StoreWorkload(c)
+    T = st.T
+    zero = torch.zeros_like(st.caches[0].len)
+    in_bytes = len(c["layers"]) * T * (512 + 128) * 2
+    out_bytes = sum(T // r for _, r in c["layers"]) * (288 + 68)
+    alg_bytes = in_bytes + out_bytes
+
+    def step(ev=None):
+        for cache in st.caches:
+            cache.len.copy_(zero)
+        if ev:
+            ev[0].record()
+        st()
+        if ev:
+            ev[1].record()
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    assert K.sync_status() == 0 and st.stored_bytes() == 890 * T
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(4)]
+    t0 = time.perf_counter()
+    for e in ev:
+        step(e)
+    torch.cuda.synchronize()
+    per = (time.perf_counter() - t0) / len(ev)
+    n = max(args.steps if args.steps < 1000 else 8, int(math.ceil(args.min_seconds / max(per, 1e-6))))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    l0 = K.launch_count()
+    t_0, t_1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        t_0.record()
+        for e in evs:
+            step(e)
+        t_1.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(t_0.elapsed_time(t_1), world)
+    assert K.sync_status() == 0
+    k_avg = sum(a.elapsed_time(b) for a, b in evs) / n
+    hbm_peak, peak_kind = peaks()
+    achieved = alg_bytes / (k_avg * 1e-3) / 1e9
+    # e2e: the step's sources copied in from pinned host memory, the lengths read back
+    h_src = [(lat.cpu().pin_memory(), ikey.cpu().pin_memory()) for lat, ikey in st.sources]
+    h_len = torch.empty(len(st.caches), dtype=torch.int32).pin_memory()
+    torch.cuda.synchronize()
+    t_s = time.perf_counter()
+    n_e = 0
+    while True:
+        for (dl, dk), (hl, hk) in zip(st.sources, h_src):
+            dl.copy_(hl, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+        for cache in st.caches:
+            cache.len.copy_(zero)
+        st()
+        for i, cache in enumerate(st.caches):
+            h_len[i:i + 1].copy_(cache.len, non_blocking=True)
+        torch.cuda.synchronize()
+        n_e += 1
+        if time.perf_counter() - t_s >= args.min_seconds:
+            break
+    dt = time.perf_counter() - t_s
+    assert K.sync_status() == 0
+    return {
+        "metric": "prefill store tokens/s", "value": world * T * n / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": n, "steps_requested": args.steps, "warmup": 6, "ms_per_step": ms / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 arithmetic (bf16 sources, fp4/fp8 codes out)", "data": "synthetic",
+        "config": {"workload": c["name"], "tokens": T, "layers": [list(x) for x in c["layers"]],
+                   "bytes_per_token_stored": st.stored_bytes() / T, "stored_gib": st.stored_bytes() / 2 ** 30,
+                   "sources": "bf16 N(0,1), 1% of channels x20, per layer",
+                   "l2": "inputs larger than L2 (5.4 GB of sources)", "parallelism": f"replicas x{world}"},
+        "step_algorithmic_bytes": alg_bytes,
+        "roofline": {"bound": "hbm", "kernel": "store_append (+ length update)", "achieved": achieved,
+                     "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": None, "kernel_ms": k_avg, "bytes_per_launch": alg_bytes},
+        "gpu_launches": int(K.launch_count() - l0),
+        "clocks": sampler.summary(),
+        "e2e": {"value": T * n_e / dt, "unit": "tokens/s", "h2d_bytes_per_step": in_bytes,
+                "d2h_bytes_per_step": 4 * len(st.caches), "steps": n_e,
+                "api": "csa2_store_append through the binding every step; sources copied in from pinned host "
+                       "memory, the lengths read back"},
+    }
+
+
 def run_ours(args, rank, world, local):
     from fp4_compressed_kv_append_b300 import configs as CF
     torch.cuda.set_device(local)
     c = CF.config(args.config)
-    line = run_append(args, rank, world, local, c) if args.config == 1 else run_decode(args, rank, world, local, c)
+    if args.config == 1:
+        line = run_append(args, rank, world, local, c)
+    elif args.config == 5:
+        line = run_store(args, rank, world, local, c)
+    else:
+        line = run_decode(args, rank, world, local, c)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(c)
     if rank == 0:

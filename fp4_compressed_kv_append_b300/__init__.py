@@ -101,16 +101,61 @@ def topk_select(scores, k: int, n=None, out=None, cand=None, stream=None):
     return out
 
 
+def _window(swa):
+    """(bf16 rows, FP8 codes, FP8 scales, W) of a window: a bf16 tensor [B, W, 512], or the
+    (codes [B, W, 512], scales [B, W, 32]) uint8 pair of swa_quant, or None."""
+    if swa is None:
+        return None, None, None, 0
+    if isinstance(swa, (tuple, list)):
+        codes, scales = swa
+        _contig(codes, scales)
+        return None, codes, scales, codes.shape[1]
+    _contig(swa)
+    return swa, None, None, swa.shape[1]
+
+
+def swa_quant(rows, stream=None):
+    """FP8 window rows of rows [..., 512] (f32 or bf16): (codes [..., 512], scales [..., 32]) uint8."""
+    _contig(rows)
+    n = rows.numel() // LATENT_DIM
+    codes = torch.empty(rows.shape, dtype=torch.uint8, device=rows.device)
+    scales = torch.empty(rows.shape[:-1] + (LATENT_DIM // 16,), dtype=torch.uint8, device=rows.device)
+    A.check(A.lib().csa2_swa_quant(_ptr(rows), _dt(rows), n, _ptr(codes), _ptr(scales), _stream(stream)),
+            "csa2_swa_quant")
+    return codes, scales
+
+
+def store_append(layers, stream=None) -> None:
+    """Append T tokens to every layer of a store in one launch. ``layers`` is a list of
+    (lat [B,T,512], ikey [B,T,128], ratio, cache, weights) with weights (w0_lat, w1_lat,
+    w0_idx, w1_idx) for ratio 2 (None for ratio 1); sources share one dtype."""
+    descs = (A.StoreLayer * len(layers))()
+    keep = []
+    for d, (lat, ikey, ratio, cache, w) in zip(descs, layers):
+        w = w or (None,) * 4
+        _contig(lat, ikey, *w)
+        view = cache.view()
+        keep.append(view)
+        d.lat, d.ikey, d.ratio = _ptr(lat), _ptr(ikey), ratio
+        d.w0_lat, d.w1_lat, d.w0_idx, d.w1_idx = (_ptr(x) for x in w)
+        d.cache = C.pointer(view)
+    lat0 = layers[0][0]
+    A.check(A.lib().csa2_store_append(descs, len(layers), _dt(lat0), lat0.shape[1], _stream(stream)),
+            "csa2_store_append")
+
+
 def sparse_latent_attn(q, cache: Cache, idx, out=None, swa=None, scale: float = DEFAULT_SCALE, stream=None):
-    """o [B, H, 512] f32 from q [B, H, 512], selected positions idx [B, k], window swa [B, W, 512] bf16."""
-    _contig(q, idx, swa, out)
+    """o [B, H, 512] f32 from q [B, H, 512], selected positions idx [B, k] and the window
+    swa (bf16 rows [B, W, 512] or the FP8 (codes, scales) pair of swa_quant)."""
+    _contig(q, idx, out)
     B, H, _ = q.shape
     k = 0 if idx is None else idx.shape[1]
-    W = 0 if swa is None else swa.shape[1]
+    bf, codes, scales, W = _window(swa)
     if out is None:
         out = torch.empty(B, H, LATENT_DIM, dtype=torch.float32, device=q.device)
-    A.check(A.lib().sparse_latent_attn(_ptr(q), _dt(q), H, scale, C.byref(cache.view()), _ptr(idx), k, _ptr(swa),
-                                       W, _ptr(out), _stream(stream)), "sparse_latent_attn")
+    A.check(A.lib().sparse_latent_attn(_ptr(q), _dt(q), H, scale, C.byref(cache.view()), _ptr(idx), k, _ptr(bf),
+                                       _ptr(codes), _ptr(scales), W, _ptr(out), _stream(stream)),
+            "sparse_latent_attn")
     return out
 
 
@@ -126,12 +171,12 @@ class Layer:
         self.idx_out = idx_out
 
     def desc(self) -> A.LayerDesc:
-        _contig(self.q, self.out, self.q_idx, self.w_idx, self.q_idx2, self.w_idx2, self.swa)
+        _contig(self.q, self.out, self.q_idx, self.w_idx, self.q_idx2, self.w_idx2)
         cache_ptr = C.pointer(self.cache.view()) if self.cache is not None else None
+        bf, codes, scales, W = _window(self.swa)
         return A.LayerDesc(self.mode, cache_ptr, _ptr(self.own_idx_codes), _ptr(self.own_idx_scales),
                            _ptr(self.q_idx), _ptr(self.w_idx), self.pool, _ptr(self.q_idx2), _ptr(self.w_idx2),
-                           _ptr(self.q), _ptr(self.swa), 0 if self.swa is None else self.swa.shape[1],
-                           _ptr(self.out), _ptr(self.idx_out))
+                           _ptr(self.q), _ptr(bf), _ptr(codes), _ptr(scales), W, _ptr(self.out), _ptr(self.idx_out))
 
 
 def workspace_size(batch: int, max_entries: int, H: int, k: int = 512, pool: int = 0, W: int = 0) -> int:
@@ -149,7 +194,7 @@ class DecodeStep:
         self.B, self.H, self.dtype = B, H, _dt(first.q)
         cap = max(L.cache.cap for L in self.layers if L.cache is not None)
         pool = max(L.pool for L in self.layers)
-        W = max(0 if L.swa is None else L.swa.shape[1] for L in self.layers)
+        W = max(_window(L.swa)[3] for L in self.layers)
         need = workspace_size(B, cap, H, k, pool, W)
         self.ws = ws if ws is not None and ws.numel() >= need else torch.empty(need, dtype=torch.uint8,
                                                                                device=first.q.device)

@@ -27,7 +27,14 @@ class LayerDesc(C.Structure):
     _fields_ = [("mode", C.c_int), ("cache", C.POINTER(CacheView)), ("own_idx_codes", C.c_void_p),
                 ("own_idx_scales", C.c_void_p), ("q_idx", C.c_void_p), ("w_idx", C.c_void_p),
                 ("pool", C.c_int32), ("q_idx2", C.c_void_p), ("w_idx2", C.c_void_p), ("q", C.c_void_p),
-                ("swa", C.c_void_p), ("W", C.c_int32), ("out", C.c_void_p), ("idx_out", C.c_void_p)]
+                ("swa", C.c_void_p), ("swa_codes", C.c_void_p), ("swa_scales", C.c_void_p), ("W", C.c_int32),
+                ("out", C.c_void_p), ("idx_out", C.c_void_p)]
+
+
+class StoreLayer(C.Structure):
+    _fields_ = [("lat", C.c_void_p), ("ikey", C.c_void_p), ("ratio", C.c_int32), ("w0_lat", C.c_void_p),
+                ("w1_lat", C.c_void_p), ("w0_idx", C.c_void_p), ("w1_idx", C.c_void_p),
+                ("cache", C.POINTER(CacheView))]
 
 
 class Csa2Error(RuntimeError):
@@ -46,7 +53,10 @@ _PROTOS = {
     "topk_select": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32,
                               C.c_void_p]),
     "sparse_latent_attn": (C.c_int, [C.c_void_p, C.c_int, C.c_int32, C.c_float, C.POINTER(CacheView), C.c_void_p,
-                                     C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
+                                     C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p,
+                                     C.c_void_p]),
+    "csa2_swa_quant": (C.c_int, [C.c_void_p, C.c_int, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "csa2_store_append": (C.c_int, [C.POINTER(StoreLayer), C.c_int32, C.c_int, C.c_int32, C.c_void_p]),
     "csa2_decode_step": (C.c_int, [C.POINTER(LayerDesc), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int,
                                    C.c_void_p, C.c_size_t, C.c_void_p]),
     "csa2_decode_step_static": (C.c_int, [C.POINTER(LayerDesc), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int,

@@ -92,11 +92,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 // Issue the gathers of the raw codes and scales of index chunk c.
 __device__ __forceinline__ void attn_prefetch_chunk(unsigned char* smem, const uint8_t* lat_codes,
@@ -128,7 +123,8 @@ template <int NPART>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, NPART == 1 ? 2 : 1)
 k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_t* __restrict__ lat_codes,
               const uint8_t* __restrict__ lat_scales, const int32_t* __restrict__ len, int64_t cap,
-              const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int W, int H,
+              const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa,
+              const uint8_t* __restrict__ swa_codes, const uint8_t* __restrict__ swa_scales, int W, int H,
               float* __restrict__ out) {
   pdl_wait_and_release();
   extern __shared__ __align__(128) unsigned char smem[];
@@ -282,7 +278,24 @@ k_sparse_attn(const void* __restrict__ q, int q_dtype, float scale, const uint8_
         __syncthreads();
         const int wr = (c - n_idx_chunks) * kAttnChunk + kk;
         ok = wr < W;
-        if (ok) {
+        if (ok && swa_codes) {  // FP8 window row: E4M3 values times the block's 2^(e - 127)
+          const size_t wrow = (size_t)b * W + wr;
+          const uint2 sv = __ldg(reinterpret_cast<const uint2*>(swa_scales + wrow * 32 + 8 * qq));
+#pragma unroll 2
+          for (int i = 0; i < 8; ++i) {  // blocks 8 qq + i: dims 128 qq + 16 i ..
+            const float f = e8m0_decode(((i < 4 ? sv.x : sv.y) >> (8 * (i & 3))) & 0xFFu);
+            const uint4 cv = __ldg(reinterpret_cast<const uint4*>(swa_codes + wrow * 512 + 128 * qq) + i);
+            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t byte2 = (cw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+              o[e] = pack_half2(e4m3_decode(byte2 & 0xFFu) * f, e4m3_decode(byte2 >> 8) * f);
+            }
+            *reinterpret_cast<uint4*>(vs + swzv(kk, 16 * qq + 2 * i)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(vs + swzv(kk, 16 * qq + 2 * i + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        } else if (ok) {
           const uint4* src = reinterpret_cast<const uint4*>(swa + ((size_t)b * W + wr) * 512 + 128 * qq);
 #pragma unroll 4
           for (int i = 0; i < 16; ++i) {

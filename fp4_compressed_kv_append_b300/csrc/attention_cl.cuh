@@ -100,7 +100,8 @@ template <int NPART>
 __global__ void __launch_bounds__(kAclThreads, 1)
 k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uint8_t* __restrict__ lat_codes,
                  const uint8_t* __restrict__ lat_scales, const int32_t* __restrict__ len, int64_t cap,
-                 const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int W, int H,
+                 const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa,
+                 const uint8_t* __restrict__ swa_codes, const uint8_t* __restrict__ swa_scales, int W, int H,
                  float* __restrict__ out, int q_early) {
   extern __shared__ __align__(1024) unsigned char acl_smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -249,6 +250,27 @@ k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uin
       const int chunk = 2 * (4 * m + qq);
       *reinterpret_cast<uint4*>(vs + acl_vidx(kk, chunk)) = make_uint4(o[0], o[1], o[2], o[3]);
       *reinterpret_cast<uint4*>(vs + acl_vidx(kk, chunk + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  } else if (kind == 2 && swa_codes) {  // FP8 window row: E4M3 values times the block's 2^(e - 127)
+    const size_t wrow = (size_t)b * W + (j - k);
+    const uint4* ss = reinterpret_cast<const uint4*>(swa_scales + wrow * 32);
+    const uint4 s0 = __ldg(ss), s1 = __ldg(ss + 1);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int g = 4 * m + qq;  // the 16-value block
+      const uint32_t sw = m < 4 ? (m == 0 ? s0.x : m == 1 ? s0.y : m == 2 ? s0.z : s0.w)
+                                : (m == 4 ? s1.x : m == 5 ? s1.y : m == 6 ? s1.z : s1.w);
+      const float f = e8m0_decode((sw >> (8 * qq)) & 0xFFu);
+      const uint4 cv = __ldg(reinterpret_cast<const uint4*>(swa_codes + wrow * 512) + g);
+      const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t byte2 = (cw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+        o[e] = pack_half2(e4m3_decode(byte2 & 0xFFu) * f, e4m3_decode(byte2 >> 8) * f);
+      }
+      *reinterpret_cast<uint4*>(vs + acl_vidx(kk, 2 * g)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(vs + acl_vidx(kk, 2 * g + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
     }
   } else if (kind == 2) {
     const uint4* src = reinterpret_cast<const uint4*>(swa + ((size_t)b * W + (j - k)) * 512);

@@ -95,10 +95,6 @@ __device__ __forceinline__ uint32_t float_order_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Score groups: the streaming indexer scan records the largest score of every
-// kGroupRows consecutive entries of a row, for the Top-k that follows it.
-constexpr int kGroupRows = 64;
-
 // Selection key of slot i with score s: (order(s) << 32) | (2^32-1 - i). Keys are
 // distinct, and a larger key is a higher score, then a lower slot.
 __device__ __forceinline__ unsigned long long topk_key(float s, uint32_t slot) {
@@ -119,6 +115,14 @@ __device__ __forceinline__ void pdl_wait_and_release() {
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint32_t smem_u32addr(const void* p) { return smem_u32(p); }
+
+// 16 bytes from global to shared memory (shared address dst), asynchronously: no
+// register holds the data, so many copies can be in flight per thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

@@ -234,12 +234,9 @@ bool scan_uses_tcgen05() {
   return v == 1;
 }
 
-// gmax (streaming mma.sync form only): [batch][cap / kGroupRows] receives the largest
-// score of every kGroupRows entries, for the Top-k after the scan; nullptr for none.
-// Returns whether the group maxima were written.
-bool launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
+void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
                  int64_t cap, const int32_t* len, const int32_t* cand, int P, float* scores, int batch,
-                 cudaStream_t s, float* gmax = nullptr) {
+                 cudaStream_t s) {
   g_launches += 1;
   CUtensorMap m;
   if (!cand && cap % kTmaRows == 0 && make_codes_map(&m, codes, (int64_t)batch * cap)) {
@@ -255,7 +252,6 @@ bool launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
     const int64_t tile_rows = scan_uses_tcgen05() ? kTmaRows : kTmaStageRows;
     t.tiles_per_seq = (cap + tile_rows - 1) / tile_rows;
     t.total_tiles = t.tiles_per_seq * batch;
-    t.gmax = scan_uses_tcgen05() ? nullptr : gmax;
     const int ev = g_scan_ev_n > 0 ? g_scan_ev_next++ % g_scan_ev_n : -1;
     if (ev >= 0) record_hook_event(g_scan_ev_before[ev], s);
     if (scan_uses_tcgen05()) {
@@ -266,7 +262,7 @@ bool launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
       else launch_scan_tma<1>(m, t, s);
     }
     if (ev >= 0) record_hook_event(g_scan_ev_after[ev], s);
-    return t.gmax != nullptr;
+    return;
   }
   ScanArgs a;
   a.q_idx = q_idx;
@@ -284,7 +280,6 @@ bool launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
   a.total_tiles = a.tiles_per_seq * batch;
   if (dt == CSA2_F32) launch_scan_gather<2>(a, s);
   else launch_scan_gather<1>(a, s);
-  return false;
 }
 
 void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,
@@ -295,39 +290,33 @@ void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, c
   g_launches += 1;
 }
 
-// Top-k of full rows whose scan recorded group maxima: one block per row bounded by the
-// maxima when k is small against the row (the bound needs at least k groups), the
-// cluster select otherwise.
-void launch_topk_rows(const float* scores, const int32_t* n, int64_t stride, int k, const float* gmax,
-                      int32_t* out, int batch, cudaStream_t s) {
-  if (gmax && k <= (int)kRxListCap && stride / kGroupRows >= 2 * (int64_t)k &&
-      stride <= (int64_t)kTgMaxGroups * kGroupRows) {
-    ensure_max_smem<k_topk_groups>((int)kTgSmem);
-    launch_k(k_topk_groups, dim3(batch), dim3(kTopkThreads), kTgSmem, s, 0u, scores, stride, n, gmax,
-             stride / kGroupRows, k, out);
-    g_launches += 1;
-    return;
-  }
-  launch_topk(scores, n, stride, k, nullptr, out, batch, s);
-}
+// Sliding-window rows of an attention launch: bf16 rows, or FP8 rows (E4M3 codes and
+// E8M0 scales), W of them per sequence.
+struct Window {
+  const uint16_t* bf16;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  int W;
+};
 
 template <int NPART>
 void launch_attn_t(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
-                   int k, const uint16_t* swa, int W, float* out, cudaStream_t s) {
+                   int k, const Window& win, float* out, cudaStream_t s) {
   ensure_max_smem<k_sparse_attn<NPART>>(kAttnSmem);
   launch_k(k_sparse_attn<NPART>, dim3(2 * (H / kAttnHeads), c.batch), dim3(kAttnThreads), kAttnSmem, s, 0u, q,
-           (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H, out);
+           (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, win.bf16, win.codes, win.scales, win.W,
+           H, out);
 }
 
 // Key-split form: one cluster of ceil((k + W) / 128) blocks per (sequence, 64 heads).
 template <int NPART>
 void launch_attn_cl(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
-                    int k, const uint16_t* swa, int W, float* out, int q_early, cudaStream_t s) {
+                    int k, const Window& win, float* out, int q_early, cudaStream_t s) {
   ensure_max_smem<k_sparse_attn_cl<NPART>>(kAclSmem);
-  const int C = (k + W + kAclKeys - 1) / kAclKeys;
+  const int C = (k + win.W + kAclKeys - 1) / kAclKeys;
   launch_k(k_sparse_attn_cl<NPART>, dim3((unsigned)(C * (H / kAclHeads)), (unsigned)c.batch), dim3(kAclThreads),
-           kAclSmem, s, (unsigned)C, q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, swa, W, H,
-           out, q_early);
+           kAclSmem, s, (unsigned)C, q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, win.bf16,
+           win.codes, win.scales, win.W, H, out, q_early);
 }
 
 // The key-split form covers 64-head groups and up to 1,024 keys per row; the
@@ -346,13 +335,13 @@ bool attn_key_split(int H, int k, int W) {
 // not write q (the decode step's Full and Reindex layers); the queries may then be
 // read before waiting for it.
 void launch_attn(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
-                 int k, const uint16_t* swa, int W, float* out, cudaStream_t s, int q_early = 0) {
-  if (attn_key_split(H, k, W)) {
-    if (dt == CSA2_F32) launch_attn_cl<2>(q, dt, H, scale, c, idx, k, swa, W, out, q_early, s);
-    else launch_attn_cl<1>(q, dt, H, scale, c, idx, k, swa, W, out, q_early, s);
+                 int k, const Window& win, float* out, cudaStream_t s, int q_early = 0) {
+  if (attn_key_split(H, k, win.W)) {
+    if (dt == CSA2_F32) launch_attn_cl<2>(q, dt, H, scale, c, idx, k, win, out, q_early, s);
+    else launch_attn_cl<1>(q, dt, H, scale, c, idx, k, win, out, q_early, s);
   } else {
-    if (dt == CSA2_F32) launch_attn_t<2>(q, dt, H, scale, c, idx, k, swa, W, out, s);
-    else launch_attn_t<1>(q, dt, H, scale, c, idx, k, swa, W, out, s);
+    if (dt == CSA2_F32) launch_attn_t<2>(q, dt, H, scale, c, idx, k, win, out, s);
+    else launch_attn_t<1>(q, dt, H, scale, c, idx, k, win, out, s);
   }
   g_launches += 1;
 }
@@ -369,6 +358,23 @@ __global__ void k_selftest_wait(uint64_t budget_ns) {
   abort_flag = 0;
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   mbar_wait_bounded_ns(b, 0u, &abort_flag, budget_ns);
+}
+
+// A window is either bf16 rows or FP8 rows (codes and scales together), never both;
+// W > 0 needs rows.
+csa2_status check_window(const uint16_t* swa, const uint8_t* codes, const uint8_t* scales, int W) {
+  if (W < 0 || W > CSA2_MAX_WINDOW || (codes == nullptr) != (scales == nullptr) || (swa && codes))
+    return CSA2_ERR_ARG;
+  if (W > 0 && !swa && !codes) return CSA2_ERR_ARG;
+  if ((swa && !aligned16(swa)) || (codes && (!aligned16(codes) || !aligned16(scales)))) return CSA2_ERR_ALIGN;
+  return CSA2_OK;
+}
+
+template <typename Tin>
+void launch_store(const StoreArgs& a, int batch, int blocks, cudaStream_t s) {
+  launch_k(k_store_append<Tin>, dim3((unsigned)blocks, (unsigned)batch), dim3(kAppendWarps * 32), 0, s, 0u, a);
+  launch_k(k_store_bump, dim3((unsigned)a.n_layers), dim3(256), 0, s, 0u, a, batch);
+  g_launches += 2;
 }
 
 }  // namespace
@@ -423,21 +429,89 @@ csa2_status topk_select(const float* scores, const int32_t* n, int64_t stride, i
 
 csa2_status sparse_latent_attn(const void* q, csa2_dtype q_dtype, int32_t H, float scale,
                                const csa2_cache_view* cache, const int32_t* idx, int32_t k, const uint16_t* swa,
-                               int32_t W, float* out, csa2_stream_t stream) {
+                               const uint8_t* swa_codes, const uint8_t* swa_scales, int32_t W, float* out,
+                               csa2_stream_t stream) {
   const csa2_status cs = check_cache(cache);
   if (cs != CSA2_OK) return cs;
   if (!q || !out || (q_dtype != CSA2_F32 && q_dtype != CSA2_BF16)) return CSA2_ERR_ARG;
   if (H != 16 && H != 32 && H != 64) return CSA2_ERR_UNSUPPORTED;
-  if (!(scale > 0.f) || k < 0 || k > CSA2_MAX_TOPK || W < 0 || W > CSA2_MAX_WINDOW) return CSA2_ERR_ARG;
-  if ((k > 0 && !idx) || (W > 0 && !swa)) return CSA2_ERR_ARG;
-  if (!aligned16(q) || !aligned16(out) || (W > 0 && !aligned16(swa))) return CSA2_ERR_ALIGN;
-  launch_attn(q, q_dtype, H, scale, *cache, idx, k, swa, W, out, (cudaStream_t)stream);
+  if (!(scale > 0.f) || k < 0 || k > CSA2_MAX_TOPK) return CSA2_ERR_ARG;
+  if (k > 0 && !idx) return CSA2_ERR_ARG;
+  const csa2_status ws = check_window(swa, swa_codes, swa_scales, W);
+  if (ws != CSA2_OK) return ws;
+  if (!aligned16(q) || !aligned16(out)) return CSA2_ERR_ALIGN;
+  launch_attn(q, q_dtype, H, scale, *cache, idx, k, Window{swa, swa_codes, swa_scales, W}, out,
+              (cudaStream_t)stream);
+  return launch_status();
+}
+
+csa2_status csa2_swa_quant(const void* rows, csa2_dtype in_dtype, int64_t n_rows, uint8_t* codes, uint8_t* scales,
+                           csa2_stream_t stream) {
+  if (in_dtype != CSA2_F32 && in_dtype != CSA2_BF16) return CSA2_ERR_ARG;
+  if (n_rows < 0 || n_rows > ((int64_t)INT32_MAX) * kSwaWarps) return CSA2_ERR_ARG;
+  if (n_rows == 0) return CSA2_OK;
+  if (!rows || !codes || !scales) return CSA2_ERR_ARG;
+  if (!aligned16(rows) || !aligned16(codes) || !aligned16(scales)) return CSA2_ERR_ALIGN;
+  const dim3 grid((unsigned)((n_rows + kSwaWarps - 1) / kSwaWarps));
+  if (in_dtype == CSA2_F32)
+    launch_k(k_swa_quant<float>, grid, dim3(kSwaWarps * 32), 0, (cudaStream_t)stream, 0u, (const float*)rows,
+             n_rows, codes, scales);
+  else
+    launch_k(k_swa_quant<uint16_t>, grid, dim3(kSwaWarps * 32), 0, (cudaStream_t)stream, 0u, (const uint16_t*)rows,
+             n_rows, codes, scales);
+  g_launches += 1;
+  return launch_status();
+}
+
+csa2_status csa2_store_append(const csa2_store_layer* layers, int32_t n_layers, csa2_dtype in_dtype, int32_t T,
+                              csa2_stream_t stream) {
+  if (!layers || n_layers < 1 || n_layers > kStoreMaxLayers) return CSA2_ERR_ARG;
+  if (in_dtype != CSA2_F32 && in_dtype != CSA2_BF16) return CSA2_ERR_ARG;
+  if (T < 0) return CSA2_ERR_ARG;
+  StoreArgs a{};
+  a.n_layers = n_layers;
+  a.T = T;
+  int batch = -1, blocks = 0;
+  for (int i = 0; i < n_layers; ++i) {
+    const csa2_store_layer& L = layers[i];
+    const csa2_status cs = check_cache(L.cache);
+    if (cs != CSA2_OK) return cs;
+    if (batch >= 0 && L.cache->batch != batch) return CSA2_ERR_ARG;
+    batch = L.cache->batch;
+    if (L.ratio != 1 && L.ratio != 2) return CSA2_ERR_ARG;
+    if (L.ratio == 2 && ((T & 1) || !L.w0_lat || !L.w1_lat || !L.w0_idx || !L.w1_idx)) return CSA2_ERR_ARG;
+    if (L.ratio == 2 && (!aligned16(L.w0_lat) || !aligned16(L.w1_lat) || !aligned16(L.w0_idx) ||
+                         !aligned16(L.w1_idx)))
+      return CSA2_ERR_ALIGN;
+    if (T > 0 && (!L.lat || !L.ikey)) return CSA2_ERR_ARG;
+    if (T > 0 && (!aligned16(L.lat) || !aligned16(L.ikey))) return CSA2_ERR_ALIGN;
+    StoreLayer& S = a.L[i];
+    S.lat = L.lat;
+    S.ikey = L.ikey;
+    S.w0l = L.w0_lat;
+    S.w1l = L.w1_lat;
+    S.w0i = L.w0_idx;
+    S.w1i = L.w1_idx;
+    S.lat_codes = L.cache->lat_codes;
+    S.lat_scales = L.cache->lat_scales;
+    S.idx_codes = L.cache->idx_codes;
+    S.idx_scales = L.cache->idx_scales;
+    S.len = L.cache->len;
+    S.cap = L.cache->cap;
+    S.ratio = L.ratio;
+    S.n_new = T / L.ratio;
+    S.block0 = blocks;
+    blocks += (S.n_new + kAppendBlockEntries - 1) / kAppendBlockEntries;
+  }
+  if (T == 0) return CSA2_OK;
+  if (in_dtype == CSA2_F32) launch_store<float>(a, batch, blocks, (cudaStream_t)stream);
+  else launch_store<uint16_t>(a, batch, blocks, (cudaStream_t)stream);
   return launch_status();
 }
 
 namespace {
 struct StepLayout {
-  size_t scores, gmax, pool, pscores, sel, total;
+  size_t scores, pool, pscores, sel, total;
 };
 
 StepLayout step_layout(int32_t batch, int64_t max_entries, int32_t H, int32_t k, int32_t pool, int32_t W) {
@@ -445,8 +519,6 @@ StepLayout step_layout(int32_t batch, int64_t max_entries, int32_t H, int32_t k,
   size_t off = 0;
   L.scores = off;
   off += round_up((size_t)batch * (size_t)max_entries * sizeof(float), 256);
-  L.gmax = off;
-  off += round_up((size_t)batch * (size_t)(max_entries / kGroupRows + 1) * sizeof(float), 256);
   L.pool = off;
   off += round_up((size_t)batch * (size_t)pool * sizeof(int32_t), 256);
   L.pscores = off;
@@ -477,8 +549,10 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
   for (int i = 0; i < n_layers; ++i) {
     const csa2_layer_desc& L = layers[i];
     if (L.mode != CSA2_FULL && L.mode != CSA2_REINDEX && L.mode != CSA2_REUSE) return CSA2_ERR_ARG;
-    if (!L.q || !L.out || L.W < 0 || L.W > CSA2_MAX_WINDOW || (L.W > 0 && !L.swa)) return CSA2_ERR_ARG;
-    if (!aligned16(L.q) || !aligned16(L.out) || (L.W > 0 && !aligned16(L.swa))) return CSA2_ERR_ALIGN;
+    if (!L.q || !L.out) return CSA2_ERR_ARG;
+    const csa2_status wst = check_window(L.swa, L.swa_codes, L.swa_scales, L.W);
+    if (wst != CSA2_OK) return wst;
+    if (!aligned16(L.q) || !aligned16(L.out)) return CSA2_ERR_ALIGN;
     if (L.mode == CSA2_FULL) {
       const csa2_status cs = check_cache(L.cache);
       if (cs != CSA2_OK) return cs;
@@ -503,14 +577,12 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
   int32_t* pool_idx = reinterpret_cast<int32_t*>(base + SL.pool);
   float* pscores = reinterpret_cast<float*>(base + SL.pscores);
   int32_t* sel = reinterpret_cast<int32_t*>(base + SL.sel);
-  float* gmax = reinterpret_cast<float*>(base + SL.gmax);
   cudaStream_t s = (cudaStream_t)stream;
   // Top-k of every entry of a cache: scores, then the cluster select
-  // (the scan records the group maxima that bound the Top-k after it)
   auto scan_and_select = [&](const void* qi, const float* wi, const uint8_t* kc, const uint8_t* ksc,
                              const csa2_cache_view* c, int32_t* out_idx) {
-    const bool g = launch_scan(qi, dtype, wi, kc, ksc, c->cap, c->len, nullptr, 0, scores, batch, s, gmax);
-    launch_topk_rows(scores, c->len, c->cap, k, g ? gmax : nullptr, out_idx, batch, s);
+    launch_scan(qi, dtype, wi, kc, ksc, c->cap, c->len, nullptr, 0, scores, batch, s);
+    launch_topk(scores, c->len, c->cap, k, nullptr, out_idx, batch, s);
   };
 
   const csa2_cache_view* main = nullptr;
@@ -523,9 +595,9 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
       main = L.cache;
       pool = L.pool;
       if (pool > 0) {
-        const bool g = launch_scan(L.q_idx, dtype, L.w_idx, main->idx_codes, main->idx_scales, main->cap,
-                                   main->len, nullptr, 0, scores, batch, s, gmax);
-        launch_topk_rows(scores, main->len, main->cap, pool, g ? gmax : nullptr, pool_idx, batch, s);
+        launch_scan(L.q_idx, dtype, L.w_idx, main->idx_codes, main->idx_scales, main->cap, main->len, nullptr, 0,
+                    scores, batch, s);
+        launch_topk(scores, main->len, main->cap, pool, nullptr, pool_idx, batch, s);
         launch_scan(L.q_idx2, dtype, L.w_idx2, main->idx_codes, main->idx_scales, main->cap, main->len, pool_idx,
                     pool, pscores, batch, s);
         launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s);
@@ -548,8 +620,8 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
           cudaSuccess)
         return CSA2_ERR_CUDA;
     }
-    launch_attn(L.q, dtype, H, 1.0f / sqrtf((float)CSA2_LATENT_DIM), *main, last, k, L.swa, L.W, L.out, s,
-                L.mode != CSA2_REUSE ? 1 : 0);
+    launch_attn(L.q, dtype, H, 1.0f / sqrtf((float)CSA2_LATENT_DIM), *main, last, k,
+                Window{L.swa, L.swa_codes, L.swa_scales, L.W}, L.out, s, L.mode != CSA2_REUSE ? 1 : 0);
   }
   return launch_status();
 }

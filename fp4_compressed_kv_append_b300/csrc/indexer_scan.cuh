@@ -330,7 +330,6 @@ constexpr int kTmaStages = CSA2_SCAN_STAGES;
 constexpr int kTmaBlocksPerSM = CSA2_SCAN_BLOCKS_PER_SM;
 constexpr int kTmaStageBytes = kTmaStageRows * 68;      // codes, then the E8M0 bytes
 constexpr int kTmaSmem = kTmaStages * kTmaStageBytes + 2 * kTmaStages * 8 + 64 + 1024;
-static_assert(kTmaWarpRows == kGroupRows, "a consumer warp's rows of a stage form one score group");
 static_assert(kTmaStageRows % kTmaRows == 0 && kTmaWarpRows % 16 == 0, "stage shape");
 static_assert(kTmaStageBytes % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled boxes");
 
@@ -345,8 +344,6 @@ struct TmaScanArgs {
   float* scores;
   int64_t tiles_per_seq;  // ceil(cap / tile rows): 256-row stages (mma.sync form), 128 (tcgen05 form)
   int64_t total_tiles;
-  float* gmax;            // [batch][cap / kGroupRows] score maximum of each group of rows, or nullptr
-                          // (mma.sync form only)
 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -530,30 +527,18 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
         // lanes t4 and t4 + 2 hold the same row: even t4 row r0 + 16 m, odd t4 that + 8
         const int64_t erow = e0 + r0 + 8 * (t4 & 1);
         float* sp = a.scores + (size_t)b * a.cap + erow;
-        float gm = -INFINITY;
         if (NPART == 1 && e0 + kTmaStageRows <= n_b) {  // every row of the stage is valid
 #pragma unroll
           for (int m = 0; m < kTmaWarpM16; ++m) {
             const float sc = scan_m16<NPART>(w[2 * m], w[2 * m + 1], sw[2 * m], sw[2 * m + 1], bf, wsel, t4);
             if (t4 < 2) sp[16 * m] = sc;
-            gm = fmaxf(gm, sc);
           }
         } else {  // the last stage of the sequence (and every stage of fp32 queries)
 #pragma unroll
           for (int m = 0; m < kTmaWarpM16; ++m) {
             const float sc = scan_m16<NPART>(w[2 * m], w[2 * m + 1], sw[2 * m], sw[2 * m + 1], bf, wsel, t4);
-            const bool ok = erow + 16 * m < n_b;
-            if (t4 < 2 && ok) sp[16 * m] = sc;
-            gm = fmaxf(gm, ok ? sc : -INFINITY);
+            if (t4 < 2 && erow + 16 * m < n_b) sp[16 * m] = sc;
           }
-        }
-        if (a.gmax) {  // the maximum of this warp's 64 rows (one score group)
-          gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
-          gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
-          gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
-          gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
-          if (lane == 0 && e0 + kGroupRows * warp < a.cap)  // (the last stage may run past cap)
-            a.gmax[(size_t)b * (a.cap / kGroupRows) + (e0 / kGroupRows) + warp] = gm;
         }
       }
       e0 += kTmaStageRows;

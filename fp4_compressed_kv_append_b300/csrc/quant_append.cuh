@@ -9,10 +9,12 @@
 // one E4M3 scale block -- and indexer channels [4l, 4l+4); eight lanes form one
 // 32-channel MXFP4 block. All loads are 16-byte vectors; every lane stores 8 bytes
 // of latent codes (one 256-byte coalesced row per warp), one scale byte and
-// 2 bytes of key codes. A warp packs up to kAppendPerWarp entries in turn, with the
-// ratio-2 merge weights of its channels loaded once into registers. E2M1 codes come
+// 2 bytes of key codes. A warp packs up to kAppendPerWarp entries in turn; the block
+// loads the ratio-2 merge weights once into shared memory. E2M1 codes come
 // from the hardware pair conversion (round to nearest even, saturating at 6, the
-// sign kept on zero), two values per instruction.
+// sign kept on zero), two values per instruction; the latent's division by its
+// scale is bracketed (e2m1_div16) so that the correctly rounded division runs only
+// next to tie points.
 #pragma once
 
 #include "common.cuh"
@@ -31,9 +33,11 @@ struct PackedLane {
   uint32_t x_code;     // the E8M0 scale of the lane's 32-channel key block
 };
 
-// Merge weights of lane l's channels (ratio 2).
-struct LaneWeights {
-  float l0[16], l1[16], i0[4], i1[4];
+// Merge weights of a block's layer (ratio 2), in shared memory, transposed so that
+// the lanes of a warp read consecutive words: [i][lane] holds latent channel 16 lane + i
+// and key channel 4 lane + i.
+struct MergeWeights {
+  float l0[16][32], l1[16][32], i0[4][32], i1[4][32];
 };
 
 // Eight E2M1 codes of v[0..7], v[2j] in the low nibble of byte j.
@@ -46,11 +50,39 @@ __device__ __forceinline__ uint32_t e2m1x8(const float* v) {
   return r;
 }
 
+// E2M1 codes of fl32(x[i] / s) for a 16-channel block (s > 0), with few divisions:
+// q = x * fl32(1/s) is within about two ulps of the quotient, so q * (1 - 2^-20) and
+// q * (1 + 2^-20) lie on either side of fl32(x / s). E2M1 rounding is monotone, so
+// where the codes of the two agree they are the code of the quotient; a block with a
+// value so close to a tie point that they differ takes the correctly rounded division.
+__device__ __forceinline__ void e2m1_div16(const float (&x)[16], float s, uint32_t& lo, uint32_t& hi) {
+  constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
+  const float r = __frcp_rn(s);
+  float a[16], c[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float q = x[i] * r;
+    a[i] = q * kDown;
+    c[i] = q * kUp;
+  }
+  const uint32_t a0 = e2m1x8(a), a1 = e2m1x8(a + 8), c0 = e2m1x8(c), c1 = e2m1x8(c + 8);
+  if (a0 == c0 && a1 == c1) {
+    lo = a0;
+    hi = a1;
+    return;
+  }
+  float q[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(x[i], s);
+  lo = e2m1x8(q);
+  hi = e2m1x8(q + 8);
+}
+
 // One entry: ratio-2 merge (optional), then both packings. Lane l of the warp.
 // Needs only the source token, not the cache position.
 template <typename Tin>
 __device__ __forceinline__ PackedLane quant_entry(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
-                                                  int ratio, const LaneWeights& W, int b, int e, int lane) {
+                                                  int ratio, const MergeWeights& W, int b, int e, int lane) {
   PackedLane P;
   const size_t tok = (size_t)b * T + (size_t)e * ratio;
 
@@ -75,9 +107,11 @@ __device__ __forceinline__ PackedLane quant_entry(const Tin* __restrict__ lat, c
   }
   if (ratio == 2) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __fadd_rn(__fmul_rn(W.l0[i], x[i]), __fmul_rn(W.l1[i], y[i]));
+    for (int i = 0; i < 16; ++i)
+      x[i] = __fadd_rn(__fmul_rn(W.l0[i][lane], x[i]), __fmul_rn(W.l1[i][lane], y[i]));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) z[i] = __fadd_rn(__fmul_rn(W.i0[i], z[i]), __fmul_rn(W.i1[i], zy[i]));
+    for (int i = 0; i < 4; ++i)
+      z[i] = __fadd_rn(__fmul_rn(W.i0[i][lane], z[i]), __fmul_rn(W.i1[i][lane], zy[i]));
   }
 
   // ---- latent: s = E4M3(amax / 6), codes E2M1(x / s)
@@ -87,12 +121,7 @@ __device__ __forceinline__ PackedLane quant_entry(const Tin* __restrict__ lat, c
   const uint32_t s_code = e4m3_encode_satfinite(__fdiv_rn(amax, 6.0f));
   const float s = e4m3_decode(s_code);
   uint32_t lo = 0, hi = 0;
-  if (s != 0.f) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __fdiv_rn(x[i], s);
-    lo = e2m1x8(x);
-    hi = e2m1x8(x + 8);
-  }
+  if (s != 0.f) e2m1_div16(x, s, lo, hi);
   P.lo = lo;
   P.hi = hi;
   P.s_code = s_code;
@@ -126,37 +155,42 @@ __device__ __forceinline__ void store_entry(const PackedLane& P, uint8_t* __rest
   if ((lane & 7) == 0) idx_scales[slot * 4 + (lane >> 3)] = (uint8_t)P.x_code;
 }
 
-// Block x of sequence b packs entries [kAppendBlockEntries x, +kAppendBlockEntries);
-// warp w takes entries w, w + kAppendWarps, ... of that range.
+// Block bx of sequence b packs entries [kAppendBlockEntries bx, +kAppendBlockEntries);
+// warp w takes entries w, w + kAppendWarps, ... of that range. With own_len (the
+// append has a single block per sequence) the block advances len itself.
 template <typename Tin>
-__global__ void __launch_bounds__(kAppendWarps * 32)
-k_quant_append(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T, int ratio,
-               const float* __restrict__ w0l, const float* __restrict__ w1l,
-               const float* __restrict__ w0i, const float* __restrict__ w1i,
-               uint8_t* __restrict__ lat_codes, uint8_t* __restrict__ lat_scales,
-               uint8_t* __restrict__ idx_codes, uint8_t* __restrict__ idx_scales,
-               int32_t* __restrict__ len, int64_t cap, int n_new) {
-  pdl_wait_and_release();
+__device__ __forceinline__ void append_block(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
+                                             int ratio, const float* __restrict__ w0l, const float* __restrict__ w1l,
+                                             const float* __restrict__ w0i, const float* __restrict__ w1i,
+                                             uint8_t* __restrict__ lat_codes, uint8_t* __restrict__ lat_scales,
+                                             uint8_t* __restrict__ idx_codes, uint8_t* __restrict__ idx_scales,
+                                             int32_t* __restrict__ len, int64_t cap, int n_new, int bx, int b,
+                                             bool own_len) {
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.y;
   const int64_t base = len[b];  // in flight while the first entry is packed
-  LaneWeights W;
-  if (ratio == 2) {
+  __shared__ MergeWeights W;
+  if (ratio == 2) {  // the block loads the weights once (16-byte vectors), transposing them
+    for (int i = threadIdx.x; i < 2 * 512 / 4; i += blockDim.x) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(i < 128 ? w0l : w1l) + (i & 127));
+      float* dst = i < 128 ? &W.l0[0][0] : &W.l1[0][0];
+      const int c0 = 4 * (i & 127);
+      const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(w0l + 16 * lane) + i);
-      const float4 c = __ldg(reinterpret_cast<const float4*>(w1l + 16 * lane) + i);
-      W.l0[4 * i] = a.x; W.l0[4 * i + 1] = a.y; W.l0[4 * i + 2] = a.z; W.l0[4 * i + 3] = a.w;
-      W.l1[4 * i] = c.x; W.l1[4 * i + 1] = c.y; W.l1[4 * i + 2] = c.z; W.l1[4 * i + 3] = c.w;
+      for (int u = 0; u < 4; ++u) dst[((c0 + u) & 15) * 32 + ((c0 + u) >> 4)] = vv[u];
     }
-    const float4 a = __ldg(reinterpret_cast<const float4*>(w0i + 4 * lane));
-    const float4 c = __ldg(reinterpret_cast<const float4*>(w1i + 4 * lane));
-    W.i0[0] = a.x; W.i0[1] = a.y; W.i0[2] = a.z; W.i0[3] = a.w;
-    W.i1[0] = c.x; W.i1[1] = c.y; W.i1[2] = c.z; W.i1[3] = c.w;
+    for (int i = threadIdx.x; i < 2 * 128 / 4; i += blockDim.x) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(i < 32 ? w0i : w1i) + (i & 31));
+      float* dst = i < 32 ? &W.i0[0][0] : &W.i1[0][0];
+      const int c0 = 4 * (i & 31);
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) dst[((c0 + u) & 3) * 32 + ((c0 + u) >> 2)] = vv[u];
+    }
+    __syncthreads();
   }
   const bool refused = base < 0 || base + n_new > cap;  // the whole append of this sequence is refused
-  if (refused && blockIdx.x == 0 && threadIdx.x == 0) set_dev_error(CSA2_ERR_BOUNDS);
-  const int e0 = blockIdx.x * kAppendBlockEntries + (threadIdx.x >> 5);
+  if (refused && bx == 0 && threadIdx.x == 0) set_dev_error(CSA2_ERR_BOUNDS);
+  const int e0 = bx * kAppendBlockEntries + (threadIdx.x >> 5);
 #pragma unroll 1
   for (int j = 0; j < kAppendPerWarp; ++j) {
     const int e = e0 + j * kAppendWarps;
@@ -165,11 +199,111 @@ k_quant_append(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
     if (!refused)
       store_entry(P, lat_codes, lat_scales, idx_codes, idx_scales, (int64_t)b * cap + base + e, lane);
   }
-  // a single block per sequence advances len itself (every thread has read it)
-  if (gridDim.x == 1) {
+  if (own_len) {  // every thread has read len
     __syncthreads();
     if (threadIdx.x == 0 && !refused) len[b] = (int32_t)(base + n_new);
   }
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kAppendWarps * 32, 3)
+k_quant_append(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T, int ratio,
+               const float* __restrict__ w0l, const float* __restrict__ w1l,
+               const float* __restrict__ w0i, const float* __restrict__ w1i,
+               uint8_t* __restrict__ lat_codes, uint8_t* __restrict__ lat_scales,
+               uint8_t* __restrict__ idx_codes, uint8_t* __restrict__ idx_scales,
+               int32_t* __restrict__ len, int64_t cap, int n_new) {
+  pdl_wait_and_release();
+  append_block(lat, ikey, T, ratio, w0l, w1l, w0i, w1i, lat_codes, lat_scales, idx_codes, idx_scales, len, cap,
+               n_new, (int)blockIdx.x, (int)blockIdx.y, gridDim.x == 1);
+}
+
+// ---------------------------------------------------------------- multi-layer store
+// csa2_store_append: T source tokens of each of up to kStoreMaxLayers layers, each
+// into its own cache with its own ratio and merge weights ("Le compte par couche":
+// layers 2, 8 and 14 at ratio 2 and layer 20 at ratio 1), in one launch: the blocks
+// of layer l are [block0, block0 + ceil(n_new / kAppendBlockEntries)) along x;
+// k_store_bump then advances every layer's lengths.
+constexpr int kStoreMaxLayers = 8;
+
+struct StoreLayer {
+  const void* lat;
+  const void* ikey;
+  const float *w0l, *w1l, *w0i, *w1i;
+  uint8_t *lat_codes, *lat_scales, *idx_codes, *idx_scales;
+  int32_t* len;
+  int64_t cap;
+  int ratio, n_new, block0;
+};
+
+struct StoreArgs {
+  StoreLayer L[kStoreMaxLayers];
+  int n_layers, T;
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(kAppendWarps * 32, 3) k_store_append(const __grid_constant__ StoreArgs a) {
+  pdl_wait_and_release();
+  int l = 0;
+  for (int i = 1; i < a.n_layers; ++i)
+    if ((int)blockIdx.x >= a.L[i].block0) l = i;
+  const StoreLayer& L = a.L[l];
+  append_block(static_cast<const Tin*>(L.lat), static_cast<const Tin*>(L.ikey), a.T, L.ratio, L.w0l, L.w1l, L.w0i,
+               L.w1i, L.lat_codes, L.lat_scales, L.idx_codes, L.idx_scales, L.len, L.cap, L.n_new,
+               (int)blockIdx.x - L.block0, (int)blockIdx.y, false);
+}
+
+// Block l advances layer l's lengths (refused appends leave len unchanged).
+__global__ void k_store_bump(const __grid_constant__ StoreArgs a, int batch) {
+  pdl_wait_and_release();
+  const StoreLayer& L = a.L[blockIdx.x];
+  for (int b = threadIdx.x; b < batch; b += blockDim.x) {
+    const int64_t l = L.len[b];
+    if (l >= 0 && l + L.n_new <= L.cap) L.len[b] = (int32_t)(l + L.n_new);
+  }
+}
+
+// ---------------------------------------------------------------- FP8 window rows
+// csa2_swa_quant: one warp per row of 512 values, lane l the 16-value block l: X =
+// floor(log2 amax) - 8 (clamped to [-127, 127]) from the exponent field, E8M0 byte
+// X + 127, value codes E4M3(x * 2^-X), nearest-even, saturating at 448 ("Le cache KV
+// en FP4", "La contrepartie : la fenetre glissante": FP8 with 512/16 scale bytes).
+constexpr int kSwaWarps = 8;
+
+template <typename Tin>
+__global__ void __launch_bounds__(kSwaWarps * 32)
+k_swa_quant(const Tin* __restrict__ rows, int64_t n_rows, uint8_t* __restrict__ codes,
+            uint8_t* __restrict__ scales) {
+  pdl_wait_and_release();
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kSwaWarps + (threadIdx.x >> 5);
+  if (r >= n_rows) return;
+  float x[16];
+  {
+    float a[8], c[8];
+    load8(rows + r * 512 + 16 * lane, a);
+    load8(rows + r * 512 + 16 * lane + 8, c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { x[i] = a[i]; x[8 + i] = c[i]; }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+  const int X = ef == 0 ? -127 : min(max(ef - 127 - 8, -127), 127);
+  // 2^-X as two exact factors (2^-X alone leaves the float range when X = -127)
+  const float f1 = __uint_as_float((uint32_t)(127 - X / 2) << 23);
+  const float f2 = __uint_as_float((uint32_t)(127 - (X - X / 2)) << 23);
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v |= e4m3_encode_satfinite((x[4 * q + u] * f1) * f2) << (8 * u);
+    w[q] = v;
+  }
+  *reinterpret_cast<uint4*>(codes + r * 512 + 16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
+  scales[r * 32 + lane] = (uint8_t)(X + 127);
 }
 
 // Advance len[b] by n_new after an append (refused appends leave len unchanged).

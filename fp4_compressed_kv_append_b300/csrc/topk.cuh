@@ -640,248 +640,4 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
     for (long long j = total + tid; j < k; j += kTopkThreads) orow[j] = -1;
 }
 
-// ---------------------------------------------------------------- group-bounded form
-// One block per row, for rows whose streaming indexer scan recorded the largest
-// score of every kGroupRows consecutive entries. L, the k-th largest of the row's
-// G group maxima, bounds the k-th largest score from below: the k groups with the
-// largest maxima hold k distinct entries >= L. Every entry >= L lies in a group
-// whose maximum is >= L, so reading only those groups finds all of them. The block
-//  1. loads the G group maxima as order keys and finds L (rx_list_select);
-//  2. lists, in order, the groups whose maximum is >= L;
-//  3. reads those groups' scores (coalesced: a warp reads two groups per load) and
-//     appends every entry with key >= L, in slot order (ordered compaction), to a
-//     list of at most kRxListCap entries;
-//  4. selects the k largest of the list and writes them in slot order
-//     (rx_finish_list).
-// Rows with at most k entries are written whole. Where the bound does not apply
-// (fewer groups than k, more than kTgMaxGroups groups, or more than kRxListCap
-// entries at or above L, as when many scores tie there), the block selects over
-// the whole row instead: histogram levels over the row's keys until one key T
-// remains or a bin is taken whole, then an ordered pass writes every key > T and
-// the first remaining slots with key T.
-constexpr int kTgMaxGroups = 16384;  // rows of up to 1,048,576 entries take the bound
-constexpr int kTgWarpLoads = 16;     // group pairs a warp holds in registers per round
-constexpr size_t kTgSmem = sizeof(TopkCtl) + 4u * kTgMaxGroups + 8u * kRxListCap;
-
-__global__ void __launch_bounds__(kTopkThreads, 1)
-k_topk_groups(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ nvec,
-              const float* __restrict__ gmax, int64_t gstride, int k, int32_t* __restrict__ out) {
-  pdl_wait_and_release();
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  TopkCtl& sh = *reinterpret_cast<TopkCtl*>(smem_raw);
-  uint32_t* gk = reinterpret_cast<uint32_t*>(smem_raw + sizeof(TopkCtl));  // group keys, then candidate groups
-  uint32_t* lkey = gk + kTgMaxGroups;                                       // the list: keys, then slots
-  uint32_t* lslot = lkey + kRxListCap;
-  const int b = blockIdx.x, tid = threadIdx.x;
-  int64_t n64 = nvec ? (int64_t)__ldg(nvec + b) : stride;
-  n64 = n64 < 0 ? 0 : (n64 > stride ? stride : n64);
-  const uint32_t n = (uint32_t)n64;
-  const float* row = scores + (size_t)b * stride;
-  int32_t* orow = out + (size_t)b * k;
-  if (n <= (uint32_t)k) {  // every entry, then -1
-    for (uint32_t i = tid; i < (uint32_t)k; i += kTopkThreads) orow[i] = i < n ? (int32_t)i : -1;
-    return;
-  }
-  const uint32_t G = (n + kGroupRows - 1) / kGroupRows;
-  if (gmax != nullptr && G >= (uint32_t)k && G <= (uint32_t)kTgMaxGroups && (((uintptr_t)row) & 15u) == 0) {
-    // ---- 1. the bound L: the k-th largest group key (or the start of a bin of exactly k)
-    const float* grow = gmax + (size_t)b * gstride;
-    uint32_t gc = 0, gmin = 0xFFFFFFFFu, gmx = 0;
-    for (uint32_t g = tid; g < G; g += kTopkThreads) {
-      const uint32_t key = float_order_key(__ldg(grow + g));
-      gk[g] = key;
-      ++gc;
-      gmin = min(gmin, key);
-      gmx = max(gmx, key);
-    }
-    block_sum_min_max(gc, gmin, gmx, sh);  // (its barriers also publish gk)
-    long long T0;
-    uint32_t te0;
-    rx_list_select(gk, G, (uint32_t)k, gmin, gmx, sh, &T0, &te0);
-    const uint32_t L = te0 == 0 ? (uint32_t)(T0 + 1) : (uint32_t)T0;
-    // ---- 2. the groups with maximum >= L, in order (thread t: groups [t gpt, t gpt + gpt))
-    const uint32_t gpt = (G + kTopkThreads - 1) / kTopkThreads;  // <= 32
-    uint32_t mine = 0;
-    for (uint32_t j = 0; j < gpt; ++j) {
-      const uint32_t g = tid * gpt + j;
-      if (g < G && gk[g] >= L) mine |= 1u << j;
-    }
-    uint32_t ncg;
-    uint32_t at = block_excl_scan((uint32_t)__popc(mine), sh, &ncg);  // (its barriers: every run is read)
-    while (mine) {
-      const int j = __ffs(mine) - 1;
-      mine &= mine - 1;
-      gk[at++] = tid * gpt + (uint32_t)j;
-    }
-    __syncthreads();
-    // ---- 3. the entries >= L of those groups, in slot order. Warp w takes a run of
-    // candidate groups, two per load (half-warp h reads group 2 i + h: lane 16 h + j
-    // takes entries 4 j .. 4 j + 3), up to kTgWarpLoads loads held in registers; the
-    // warps' counts give their offsets, then each warp writes its run in order.
-    const int lane = tid & 31, wid = tid >> 5, half = lane >> 4, j4 = lane & 15;
-    uint32_t total = 0;
-    bool fits = true;
-    for (uint32_t c0 = 0; c0 < ncg; c0 += 2u * kTgWarpLoads * kTopkWarps) {  // rounds of candidate groups
-      const uint32_t cr = min(ncg - c0, 2u * kTgWarpLoads * kTopkWarps);
-      const uint32_t per_w = (cr + kTopkWarps - 1) / kTopkWarps;             // groups of this warp's run
-      const uint32_t w0 = c0 + min((uint32_t)wid * per_w, cr), w1 = c0 + min((uint32_t)(wid + 1) * per_w, cr);
-      // first slot of this lane's four entries of pair i (0xFFFFFFFF past the run)
-      auto slot0_of = [&](int i) -> uint32_t {
-        const uint32_t ci = w0 + 2u * (uint32_t)i + (uint32_t)half;
-        return ci < w1 ? gk[ci] * kGroupRows + 4u * j4 : 0xFFFFFFFFu;
-      };
-      float4 v[kTgWarpLoads];
-#pragma unroll
-      for (int i = 0; i < kTgWarpLoads; ++i) {
-        const uint32_t s0 = slot0_of(i);
-        v[i] = s0 < n ? __ldg(reinterpret_cast<const float4*>(row + s0)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      uint32_t cnt = 0;
-#pragma unroll
-      for (int i = 0; i < kTgWarpLoads; ++i) {
-        const uint32_t s0 = slot0_of(i);
-        const float x[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) cnt += (s0 + u < n && float_order_key(x[u]) >= L) ? 1u : 0u;
-      }
-      const uint32_t wcnt = __reduce_add_sync(0xffffffffu, cnt);
-      if (lane == 0) sh.warp_a[wid] = wcnt;
-      __syncthreads();
-      uint32_t woff = 0, rtot = 0;
-#pragma unroll
-      for (int q = 0; q < kTopkWarps; ++q) {
-        const uint32_t t = sh.warp_a[q];
-        woff += q < wid ? t : 0u;
-        rtot += t;
-      }
-      __syncthreads();
-      if (total + rtot > kRxListCap) {  // (the same decision in every thread)
-        fits = false;
-        break;
-      }
-      // write this warp's run in order: pair i, lower half first, lanes in order, u in order
-      uint32_t p = total + woff;
-#pragma unroll
-      for (int i = 0; i < kTgWarpLoads; ++i) {
-        const uint32_t s0 = slot0_of(i);
-        const float x[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        uint32_t f = 0;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) f |= (s0 + u < n && float_order_key(x[u]) >= L) ? 1u << u : 0u;
-        const uint32_t c = (uint32_t)__popc(f);
-        uint32_t incl = c;  // inclusive prefix over the warp's lanes
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        uint32_t q = p + incl - c;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if ((f >> u) & 1u) {
-            lkey[q] = float_order_key(x[u]);
-            lslot[q] = s0 + (uint32_t)u;
-            ++q;
-          }
-        }
-        p += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      total += rtot;
-    }
-    if (fits && total >= (uint32_t)k) {
-      if (tid < kTopkCluster) {  // one run: the whole list, in slot order
-        sh.seg_off[tid] = 0;
-        sh.seg_cnt[tid] = tid == 0 ? total : 0u;
-      }
-      __syncthreads();
-      // ---- 4. the k largest of the list, written in slot order
-      rx_finish_list(lkey, lslot, total, (uint32_t)k, L, gmx, sh, k, nullptr, orow);
-      return;
-    }
-    __syncthreads();  // the whole-row path below reuses the shared memory
-  }
-
-  // ---- whole row: thread t takes a run of a multiple of 4 slots, read from global memory
-  const uint32_t run = (((n + kTopkThreads - 1) / kTopkThreads) + 3) & ~3u;
-  RxRow R;
-  R.row = row;
-  R.crow = nullptr;
-  R.s_begin = min(run * (uint32_t)tid, n);
-  R.s_end = min(R.s_begin + run, n);
-  R.vec = (((uintptr_t)row) & 15u) == 0;
-  R.kept = false;
-  uint32_t c = 0, klo = 0xFFFFFFFFu, khi = 0;
-  rx_visit(R, nullptr, nullptr, [&](uint32_t, uint32_t key) {
-    ++c;
-    klo = min(klo, key);
-    khi = max(khi, key);
-  });
-  block_sum_min_max(c, klo, khi, sh);
-  long long Tc = -1;
-  uint32_t take_eq = 0;
-  uint32_t need = (uint32_t)k;
-  constexpr int BPT = kRxBins / kTopkThreads;  // bins per thread, highest first
-  for (;;) {
-    const uint32_t shift = rx_shift(khi - klo);
-    const uint32_t lo = klo, hi = khi;
-    for (int j = tid; j < kRxBins; j += kTopkThreads) sh.hist[0][j] = 0;
-    __syncthreads();
-    rx_visit(R, nullptr, nullptr, [&](uint32_t, uint32_t key) {
-      if (key - lo <= hi - lo) atomicAdd(&sh.hist[0][(key - lo) >> shift], 1u);
-    });
-    __syncthreads();
-    const int btop = kRxBins - 1 - BPT * tid;
-    uint32_t own = 0;
-#pragma unroll
-    for (int j = 0; j < BPT; ++j) own += sh.hist[0][btop - j];
-    uint32_t tot;
-    const uint32_t above = block_excl_scan(own, sh, &tot);
-    if (above < need && above + own >= need) {
-      uint32_t acc = above;
-#pragma unroll
-      for (int j = 0; j < BPT; ++j) {
-        const uint32_t h = sh.hist[0][btop - j];
-        if (acc < need && acc + h >= need) {
-          sh.bc[0] = (uint32_t)(btop - j);
-          sh.bc[1] = acc;
-          sh.bc[2] = h;
-        }
-        acc += h;
-      }
-    }
-    __syncthreads();
-    const uint32_t B = sh.bc[0], above_b = sh.bc[1], cnt_b = sh.bc[2];
-    __syncthreads();
-    const uint32_t blo = lo + (B << shift);
-    if (above_b + cnt_b == need) {  // the bin is taken whole: every key >= blo
-      Tc = (long long)blo - 1;
-      take_eq = 0;
-      break;
-    }
-    if (shift == 0) {  // a bin of one key
-      Tc = (long long)blo;
-      take_eq = need - above_b;
-      break;
-    }
-    need -= above_b;
-    klo = blo;
-    khi = min(hi, blo + ((1u << shift) - 1u));
-  }
-  // ordered output: every key > Tc and the first take_eq slots with key == Tc
-  uint32_t gt = 0, eq = 0;
-  rx_visit(R, nullptr, nullptr, [&](uint32_t, uint32_t key) {
-    gt += (long long)key > Tc;
-    eq += (long long)key == Tc;
-  });
-  unsigned long long tot64;
-  const unsigned long long ex64 = block_excl_scan64(((unsigned long long)gt << 32) | eq, sh, &tot64);
-  uint32_t eqi = (uint32_t)ex64;
-  uint32_t pos = (uint32_t)(ex64 >> 32) + min(take_eq, eqi);
-  rx_visit(R, nullptr, nullptr, [&](uint32_t sl, uint32_t key) {
-    bool take = (long long)key > Tc;
-    if ((long long)key == Tc) take = eqi++ < take_eq;
-    if (take && pos < (uint32_t)k) orow[pos++] = (int32_t)sl;
-  });
-}
-
 }  // namespace csa2

@@ -78,9 +78,11 @@ def outlier_tokens(seed: int, seq: int, T: int, device="cpu"):
     return lat.to(torch.bfloat16), ikey.to(torch.bfloat16)
 
 
-def merge_weights(seed: int, device="cpu"):
-    """U(0,1) per-channel merge weights: (w0_lat, w1_lat [512], w0_idx, w1_idx [128]) fp32."""
-    g = generator(seed, "merge-weights", device=device)
+def merge_weights(seed: int, device="cpu", layer=None):
+    """U(0,1) per-channel merge weights: (w0_lat, w1_lat [512], w0_idx, w1_idx [128]) fp32
+    (``layer``: the weights of one source layer of a multi-layer store)."""
+    g = generator(seed, "merge-weights", device=device) if layer is None else \
+        generator(seed, "merge-weights", layer, device=device)
     w = torch.rand(2 * (LAT + IDX), generator=g, device=device)
     return w[:LAT], w[LAT:2 * LAT], w[2 * LAT:2 * LAT + IDX], w[2 * LAT + IDX:]
 

@@ -116,6 +116,52 @@ CSA2_API csa2_status kv_quant_append(const void* lat, const void* ikey, csa2_dty
                             const float* w0_idx, const float* w1_idx,
                             const csa2_cache_view* cache /* host struct */, csa2_stream_t stream);
 
+/* One source layer of csa2_store_append (host struct holding device pointers). */
+typedef struct {
+  const void* lat;               /* [batch][T][512] */
+  const void* ikey;              /* [batch][T][128] */
+  int32_t ratio;                 /* 1 or 2 */
+  const float* w0_lat;           /* ratio 2: merge weights as in kv_quant_append */
+  const float* w1_lat;
+  const float* w0_idx;
+  const float* w1_idx;
+  const csa2_cache_view* cache;  /* host ptr: this layer's cache */
+} csa2_store_layer;
+
+/*
+ * csa2_store_append -- write T source tokens into each of up to 8 layers' caches in
+ * one launch.
+ *
+ * "Le cache KV en FP4", section "Le compte par couche" (table and eq. 890): the
+ * global cache holds four source layers, 2, 8 and 14 at ratio 2 (178 B per token)
+ * and 20 at ratio 1 (356 B per token), 890 B per token in all; "Ce que cela donne
+ * aux echelles reelles": 0.87 GiB at 1,048,576 tokens.
+ *   layers: host array of n_layers (1..8) descriptors; every cache has the same
+ *     batch. Each layer packs exactly as kv_quant_append does with its own ratio
+ *     and weights (T even when any layer has ratio 2) and appends T/ratio entries
+ *     at its len[b]; an append past a layer's cap writes nothing for that layer and
+ *     sequence and records CSA2_ERR_BOUNDS.
+ *   Sources and weights 16-byte aligned (CSA2_ERR_ALIGN otherwise).
+ */
+CSA2_API csa2_status csa2_store_append(const csa2_store_layer* layers, int32_t n_layers, csa2_dtype in_dtype,
+                                       int32_t T, csa2_stream_t stream);
+
+/*
+ * csa2_swa_quant -- pack sliding-window rows as FP8.
+ *
+ * "Le cache KV en FP4", section "La contrepartie : la fenetre glissante": each
+ * layer keeps its 128-token window in FP8, 512 values plus 512/16 scale bytes per
+ * token (40 x 128 x (512 + 512/16) = 2,66 MiB per sequence). The page leaves the
+ * scale format open; this library reads it as a power-of-two (E8M0) scale per 16
+ * values: X = floor(log2 amax) - 8 clamped to [-127, 127], scale byte X + 127,
+ * value codes E4M3(x * 2^-X) (nearest-even, saturating at 448; amax = 0 gives
+ * X = -127 and +0 codes).
+ *   rows [n_rows][512] (in_dtype f32 or bf16); codes [n_rows][512] u8 (E4M3 fn);
+ *   scales [n_rows][32] u8 (E8M0). All 16-byte aligned.
+ */
+CSA2_API csa2_status csa2_swa_quant(const void* rows, csa2_dtype in_dtype, int64_t n_rows, uint8_t* codes,
+                                    uint8_t* scales, csa2_stream_t stream);
+
 /*
  * indexer_score -- score cached entries with the 4-head indexer.
  *
@@ -161,14 +207,19 @@ CSA2_API csa2_status topk_select(const float* scores, const int32_t* n, int64_t 
  *   cache: the main KV (only lat_codes/lat_scales/len/cap are read).
  *   idx [batch][k] positions, -1 skipped; 0 <= k <= CSA2_MAX_TOPK. A position
  *     >= len[b] is skipped and records CSA2_ERR_BOUNDS.
- *   swa [batch][W][512] bf16 window rows ("La contrepartie : la fenetre
- *     glissante"; "Troisiemement": 128 tokens), NULL with W = 0.
+ *   The window ("La contrepartie : la fenetre glissante"; "Troisiemement": 128
+ *     tokens): W rows per sequence, either bf16 rows swa [batch][W][512] or FP8
+ *     rows swa_codes [batch][W][512] + swa_scales [batch][W][32] (the csa2_swa_quant
+ *     format); NULL pointers with W = 0. Window values enter the tensor cores as
+ *     fp16: they must lie within its range (|x| <= 65504), and magnitudes below
+ *     about 2^-21 are rounded to its grid.
  *   out [batch][H][512] f32. With no key at all the output row is zero.
  *   The partial results of a row stay on chip: no scratch.
  */
 CSA2_API csa2_status sparse_latent_attn(const void* q, csa2_dtype q_dtype, int32_t H, float scale,
                                const csa2_cache_view* cache /* host struct */,
-                               const int32_t* idx, int32_t k, const uint16_t* swa, int32_t W,
+                               const int32_t* idx, int32_t k, const uint16_t* swa,
+                               const uint8_t* swa_codes, const uint8_t* swa_scales, int32_t W,
                                float* out, csa2_stream_t stream);
 
 /* One layer of a decode step (host struct holding device pointers). */
@@ -183,8 +234,10 @@ typedef struct {
   const void* q_idx2;            /* FULL with pool: second indexer [batch][4][128] */
   const float* w_idx2;           /* FULL with pool: [batch][4] */
   const void* q;                 /* [batch][H][512] */
-  const uint16_t* swa;           /* [batch][W][512] bf16 or NULL */
-  int32_t W;                     /* window rows (0 if swa == NULL) */
+  const uint16_t* swa;           /* [batch][W][512] bf16 window rows, or NULL */
+  const uint8_t* swa_codes;      /* or FP8 window rows: [batch][W][512] E4M3 ... */
+  const uint8_t* swa_scales;     /* ... and [batch][W][32] E8M0 (csa2_swa_quant); NULL for bf16 */
+  int32_t W;                     /* window rows (0 without a window) */
   float* out;                    /* [batch][H][512] f32 */
   int32_t* idx_out;              /* optional [batch][k]: receives the positions attended with */
 } csa2_layer_desc;
@@ -243,8 +296,8 @@ CSA2_API csa2_status csa2_decode_step_static(const csa2_layer_desc* layers, int3
                                              int32_t H, int32_t k, csa2_dtype dtype, csa2_stream_t stream);
 
 /* Scratch bytes of csa2_decode_step for these sizes (max_entries = cap): scores
- * [batch][max_entries] f32, the largest score of every 64 entries [batch][max_entries
- * / 64 + 1] f32, pool positions and scores [batch][pool], selection [batch][k]. */
+ * [batch][max_entries] f32, pool positions and scores [batch][pool], selection
+ * [batch][k]. */
 CSA2_API size_t csa2_workspace_size(int32_t batch, int64_t max_entries, int32_t H, int32_t k, int32_t pool,
                            int32_t W);
 

@@ -53,6 +53,8 @@ IDX_SCALE_BYTES = INDEXER_DIM // INDEXER_BLOCK     # 4
 TOPK = 512                # [CTX] "Deuxiemement": new Top-512 indices
 HSI_POOL = 16384          # [CTX] "Deuxiemement": candidates limited to 16,384 positions
 SWA_WINDOW = 128          # [CTX] "Troisiemement": 128-token sliding window
+SWA_BLOCK = 16            # [FP4] "La contrepartie": 512/16 scale bytes per FP8 window token
+E4M3_EMAX = 8             # largest E4M3 exponent: 448 = 1.75 * 2**8
 
 
 # =========================================================== a1: ratio-2 merge
@@ -388,6 +390,55 @@ def decode_step(layers, k: int = TOPK):
         outs.append(out)
         idxs.append(last_idx.copy())
     return outs, idxs
+
+
+# ===================================================== FP8 sliding-window rows
+def quantize_swa(x: np.ndarray):
+    """Quantise window rows [n, 512] to FP8: E4M3 values with one scale byte per 16.
+
+    [FP4] "La contrepartie : la fenetre glissante": every layer keeps its 128-token
+    window in FP8, 512 values plus 512/16 scale bytes per token (eq. 2,66 Mio). The
+    page leaves the scale format open. Reading: a power-of-two E8M0 scale per 16
+    values, as in the MX conversion: X = floor(log2 amax) - 8 (the largest E4M3
+    exponent), clamped to [-127, 127]; byte X + 127; value code = E4M3(x * 2**-X),
+    nearest-even, saturating at 448. amax = 0 gives X = -127 and +0 codes.
+    Returns (codes [n, 512] uint8, e8m0 [n, 32] uint8).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    n = x.shape[0]
+    blocks = x.reshape(n, LATENT_DIM // SWA_BLOCK, SWA_BLOCK).astype(np.float64)
+    amax = np.abs(blocks).max(axis=-1)
+    pos = amax > 0
+    X = np.where(pos, F.floor_log2(np.where(pos, amax, 1.0)) - E4M3_EMAX, -127)
+    X = np.clip(X, -127, 127).astype(np.int64)
+    codes = F.e4m3_encode(np.ldexp(blocks, -X[..., None])).reshape(n, LATENT_DIM)
+    return codes.astype(np.uint8), (X + 127).astype(np.uint8)
+
+
+def dequantize_swa(codes: np.ndarray, e8m0: np.ndarray) -> np.ndarray:
+    """FP8 window rows (E4M3 codes [n, 512], E8M0 scales [n, 32]) -> float64 [n, 512] (exact)."""
+    n = codes.shape[0]
+    v = F.e4m3_decode(codes).reshape(n, LATENT_DIM // SWA_BLOCK, SWA_BLOCK)
+    return (v * F.e8m0_decode(e8m0)[..., None]).reshape(n, LATENT_DIM)
+
+
+# ===================================================== multi-layer store
+def store_entries(layer_sources, layers=None, weights=None):
+    """Pack T source tokens into the global cache of every source layer.
+
+    [FP4] "Le compte par couche": the global cache holds four source layers, 2, 8 and
+    14 at ratio 2 and 20 at ratio 1; a ratio-m layer stores one entry per m tokens.
+    ``layer_sources`` is a list of (lat [T, 512], ikey [T, 128]) per layer, ``layers``
+    the (number, zone, ratio) rows (default SOURCE_LAYERS) and ``weights`` the merge
+    weights (w0_lat, w1_lat, w0_idx, w1_idx) of each ratio-2 layer (None for ratio 1).
+    Returns one (lat_codes, lat_scales, idx_codes, idx_scales) tuple per layer.
+    """
+    layers = SOURCE_LAYERS if layers is None else layers
+    weights = [None] * len(layers) if weights is None else weights
+    out = []
+    for (lat, ikey), (_, _, ratio), w in zip(layer_sources, layers, weights):
+        out.append(encode_entries(lat, ikey, ratio, *(w if w is not None else [None] * 4)))
+    return out
 
 
 # ===================================================== footprint arithmetic

@@ -492,3 +492,49 @@ def check_decode_modes(decode_step, FULL, REINDEX, REUSE):
         assert [list(idxs[i][b]) for i in range(4)] == [e0, e1, e2, e2]
         for i, (qq, sel) in enumerate([(q[0], e0), (q[1], e1), (q[2], e2), (q[1], e2)]):
             assert np.allclose(outs[i][b], sdpa_ref(qq[b], lat[sel]), rtol=1e-11, atol=1e-12), i
+
+
+# ------------------------------------------------------------ FP8 window pins
+def swa_block_brute(block):
+    """Exact restatement of one 16-value FP8 window block: X = floor(log2 amax) - 8
+    (by exact rational comparison), E4M3 of x * 2^-X by exhaustive nearest search."""
+    xs = [Fraction(float(x)) for x in block]
+    amax = max(abs(x) for x in xs)
+    if amax == 0:
+        return [0x80 if np.signbit(np.float32(x)) else 0 for x in block], 0
+    e = 0
+    while Fraction(2) ** (e + 1) <= amax:
+        e += 1
+    while Fraction(2) ** e > amax:
+        e -= 1
+    X = max(min(e - 8, 127), -127)
+    codes = []
+    for x, xf in zip(block, xs):
+        v = xf * Fraction(2) ** -X
+        c = e4m3_brute(v)
+        if v == 0 and np.signbit(np.float32(x)):
+            c |= 0x80
+        codes.append(c)
+    return codes, X + 127
+
+
+def check_quantize_swa(quantize_swa, dequantize_swa):
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal((6, 512)) * np.exp(rng.uniform(-6, 6, (6, 1)))).astype(np.float32)
+    x[0, :16] = 0.0
+    x[0, 16:32] = -0.0
+    x[1, 32:48] *= 1e-30
+    x[2, 48:64] = np.float32(1e30)
+    codes, scales = quantize_swa(x)
+    assert codes.shape == (6, 512) and scales.shape == (6, 32)
+    assert codes.nbytes / 6 + scales.nbytes / 6 == 512 + 32  # 544 bytes per window token
+    for r in range(6):
+        for blk in range(32):
+            c, s = swa_block_brute(x[r, 16 * blk:16 * blk + 16])
+            assert list(codes[r, 16 * blk:16 * blk + 16]) == c and scales[r, blk] == s, (r, blk)
+    d = dequantize_swa(codes, scales)
+    c2, s2 = quantize_swa(d.astype(np.float32))
+    assert np.array_equal(c2, codes) and np.array_equal(s2, scales)  # idempotent
+    # the E4M3 decode of the codes times 2^(e - 127) is the dequantised value
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(d, ref * np.repeat(np.exp2(scales.astype(np.float64) - 127), 16, axis=1))

@@ -37,11 +37,11 @@ def test_status_strings():
 
 def test_workspace_sizes():
     L = A.lib()
-    # the decode step needs the scores, the group maxima, the pool and the selection
+    # the decode step needs the scores, the pool and the selection
     total = L.csa2_workspace_size(32, 131072, 64, 512, 0, 0)
-    assert total >= 32 * 131072 * 4 + 32 * 2048 * 4 + 32 * 512 * 4
+    assert total >= 32 * 131072 * 4 + 32 * 512 * 4
     pooled = L.csa2_workspace_size(8, 524288, 64, 512, 16384, 0)
-    assert pooled >= 8 * 524288 * 4 + 8 * 8192 * 4 + 2 * 8 * 16384 * 4 + 8 * 512 * 4
+    assert pooled >= 8 * 524288 * 4 + 2 * 8 * 16384 * 4 + 8 * 512 * 4
 
 
 def _fake_cache(cap=256, batch=2, base=0x10000):
@@ -69,9 +69,9 @@ def test_host_validation_rejects_before_any_launch():
     assert L.topk_select(0x100, None, 1000, 0, None, 0x200, 1, None) == A.ERR_ARG
     assert L.topk_select(0x100, None, 1000, 16385, None, 0x200, 1, None) == A.ERR_ARG
     # attention: head count, a window without rows
-    assert L.sparse_latent_attn(0x100, A.BF16, 48, 0.04, C.byref(cv), 0x200, 512, None, 0, 0x300,
+    assert L.sparse_latent_attn(0x100, A.BF16, 48, 0.04, C.byref(cv), 0x200, 512, None, None, None, 0, 0x300,
                                 None) == A.ERR_UNSUPPORTED
-    assert L.sparse_latent_attn(0x100, A.BF16, 64, 0.04, C.byref(cv), 0x200, 512, None, 5, 0x300,
+    assert L.sparse_latent_attn(0x100, A.BF16, 64, 0.04, C.byref(cv), 0x200, 512, None, None, None, 5, 0x300,
                                 None) == A.ERR_ARG
     # bounded-wait self-test: a limit over one second is refused before any launch
     assert L.csa2_selftest_wait_timeout(1_000_000_001, None) == A.ERR_ARG
@@ -97,3 +97,34 @@ def test_decode_step_validation():
 
 def test_launch_counter_starts_at_zero_without_gpu_work():
     assert A.lib().csa2_launch_count() == 0
+
+
+def test_store_append_and_window_validation():
+    L = A.lib()
+    cv, cv3 = _fake_cache(), _fake_cache(batch=3)
+    lay = (A.StoreLayer * 2)()
+    for d in lay:
+        d.lat, d.ikey, d.ratio, d.cache = 0x1000, 0x2000, 1, C.pointer(cv)
+    assert L.csa2_store_append(lay, 0, A.BF16, 4, None) == A.ERR_ARG        # no layer
+    assert L.csa2_store_append(lay, 9, A.BF16, 4, None) == A.ERR_ARG        # more than 8
+    lay[1].ratio = 2                                                        # ratio 2 without weights
+    assert L.csa2_store_append(lay, 2, A.BF16, 4, None) == A.ERR_ARG
+    lay[1].w0_lat = lay[1].w1_lat = lay[1].w0_idx = lay[1].w1_idx = 0x3000
+    assert L.csa2_store_append(lay, 2, A.BF16, 5, None) == A.ERR_ARG        # odd T at ratio 2
+    lay[1].w1_idx = 0x3004
+    assert L.csa2_store_append(lay, 2, A.BF16, 4, None) == A.ERR_ALIGN      # unaligned weights
+    lay[1].w1_idx = 0x3000
+    lay[1].cache = C.pointer(cv3)
+    assert L.csa2_store_append(lay, 2, A.BF16, 4, None) == A.ERR_ARG        # batch mismatch
+    lay[1].cache = C.pointer(cv)
+    assert L.csa2_store_append(lay, 2, A.BF16, 0, None) == A.OK             # T = 0: nothing to do
+    # FP8 window rows: null outputs, unaligned rows, bad dtype
+    assert L.csa2_swa_quant(0x100, A.BF16, 4, None, 0x300, None) == A.ERR_ARG
+    assert L.csa2_swa_quant(0x101, A.BF16, 4, 0x200, 0x300, None) == A.ERR_ALIGN
+    assert L.csa2_swa_quant(0x100, 7, 4, 0x200, 0x300, None) == A.ERR_ARG
+    assert L.csa2_swa_quant(None, A.BF16, 0, None, None, None) == A.OK
+    # attention: a window given both as bf16 and FP8 rows, or FP8 codes without scales
+    assert L.sparse_latent_attn(0x100, A.BF16, 64, 0.04, C.byref(cv), 0x200, 512, 0x400, 0x500, 0x600, 8, 0x300,
+                                None) == A.ERR_ARG
+    assert L.sparse_latent_attn(0x100, A.BF16, 64, 0.04, C.byref(cv), 0x200, 512, None, 0x500, None, 8, 0x300,
+                                None) == A.ERR_ARG

@@ -22,6 +22,20 @@ def _oracle_rows(c, b, stream="tokens"):
     return OP.encode_rows(np_(lat), np_(ikey), c["ratio"], w)
 
 
+def _window_ref(inp, b):
+    """The oracle's window rows of sequence b, [1, W, 512] float64: the bf16 rows, or
+    their FP8 packing by the oracle (the GPU's packed bytes must equal it)."""
+    if inp["swa"] is None:
+        return None
+    rows = np_(inp["swa"][b])
+    if inp.get("swa_fp8") is None:
+        return rows[None].astype(np.float64)
+    codes, scales = O.quantize_swa(rows)
+    gc, gs = inp["swa_fp8"]
+    assert np.array_equal(np_(gc[b]), codes) and np.array_equal(np_(gs[b]), scales), "FP8 window bytes"
+    return O.dequantize_swa(codes, scales)[None]
+
+
 def _check_sequence(wl: CF.DecodeWorkload, b: int):
     """Sequence b of a decode step against the oracle: the packed cache rows
     bit-exact; every Full/Reindex selection equal to the oracle's up to near-ties
@@ -42,7 +56,7 @@ def _check_sequence(wl: CF.DecodeWorkload, b: int):
     layers = []
     for li, mode in enumerate(c["modes"]):
         inp = wl.inputs[li]
-        L = dict(mode=mode, q=f64(inp["q"]), swa=f64(inp["swa"]))
+        L = dict(mode=mode, q=f64(inp["q"]), swa=_window_ref(inp, b))
         if mode == O.FULL:
             L.update(cache=host, q_idx=f64(inp["q_idx"]), w_idx=f64(inp["w_idx"]), pool=c["pool"],
                      q_idx2=f64(inp["q_idx2"]), w_idx2=f64(inp["w_idx2"]))
@@ -79,7 +93,7 @@ def _check_sequence(wl: CF.DecodeWorkload, b: int):
                 swaps += Hh.assert_topk_match(got_idx, idxs[li][0], s, where=where)
         else:
             assert np.array_equal(got_idx, np_(wl.indices[li - 1][b])), where
-        swa = f64(inp["swa"])
+        swa = _window_ref(inp, b)
         ref = O.attend(f64(inp["q"])[0], host.lat_codes[0], host.lat_scales[0], got_idx,
                        None if swa is None else swa[0])
         err = Hh.attn_rel_err(np_(wl.outputs[li][b]), ref)
@@ -133,6 +147,11 @@ def test_pool_then_reindex_own_keys_then_reuse():
 
 def test_pool_then_reindex_shared_keys_then_reuse():
     _run(3, B=2, tokens=2 * 20000, modes=(CF.FULL, CF.REINDEX, CF.REUSE), W=0, reindex_keys="shared")
+
+
+def test_config4_reduced_fp8_window():
+    """The decoder group with its windows packed as FP8 (E4M3, one E8M0 scale per 16)."""
+    _run(4, B=3, tokens=3000, window="fp8")
 
 
 def test_reindex_with_the_full_layers_keys():

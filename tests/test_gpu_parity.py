@@ -142,6 +142,24 @@ def test_append_argument_errors():
         K.kv_quant_append(lat[None], ikey[None], 3, cache)
 
 
+# ============================================================== FP8 window rows
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_swa_quant_bit_exact(dtype):
+    """FP8 window rows (E4M3 values, one E8M0 scale per 16) equal the oracle's, with
+    zero, negative-zero, tiny, huge and saturating blocks."""
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((300, 512)) * np.exp(rng.uniform(-8, 8, (300, 1)))).astype(np.float32)
+    x[0, :16], x[0, 16:32], x[1, 32:48] = 0.0, -0.0, 2.0 ** -140
+    x[2, 48:64] = np.float32(3e38)
+    x[3, 64:80] = np.float32(500.0) * (1 + np.arange(16) / 64)  # above 448 times 2^X: saturates
+    t = torch.from_numpy(x).to(dtype).cuda()
+    codes, scales = K.swa_quant(t)
+    torch.cuda.synchronize()
+    rc, rs = O.quantize_swa(np_(t))
+    assert np.array_equal(np_(codes), rc) and np.array_equal(np_(scales), rs)
+    assert K.sync_status() == 0
+
+
 # ============================================================== indexer scores
 def _small_cache(B, N, seed=1, cap=None):
     cap = cap or ((N + 127) // 128) * 128
@@ -265,6 +283,27 @@ def test_attention_within_2e3(H, k, W, dtype):
                        None if swa is None else np_(swa[b]).astype(np.float64))
         err = Hh.attn_rel_err(np_(out[b]), ref)
         assert err <= Hh.ATTN_TOL, (b, err)
+
+
+@pytest.mark.parametrize("H,k,W", [(64, 512, 128), (64, 0, 77), (16, 300, 40), (64, 1000, 24)])
+def test_attention_fp8_window_within_2e3(H, k, W):
+    """Window rows given as FP8 (the csa2_swa_quant format): the attention equals the
+    oracle's over the dequantised rows (key-split form at H = 64, chunked at 16)."""
+    B, N = 2, 1500
+    cache, host = _small_cache(B, N, seed=4)
+    q, _, _ = WL.queries(5, 0, B, H, dtype=torch.bfloat16, device="cuda")
+    rows = WL.window(5, 0, B, W, device="cuda")
+    codes, scales = K.swa_quant(rows)
+    rng = np.random.default_rng(H + k + W)
+    idx = np.stack([np.sort(rng.choice(N, k, replace=False)) for _ in range(B)]).astype(np.int32) if k else None
+    out = K.sparse_latent_attn(q, cache, torch.from_numpy(idx).cuda() if k else None, swa=(codes, scales))
+    torch.cuda.synchronize()
+    assert K.sync_status() == 0
+    for b in range(B):
+        rc, rs = O.quantize_swa(np_(rows[b]))
+        ref = O.attend(np_(q[b]).astype(np.float64), host.lat_codes[b], host.lat_scales[b],
+                       idx[b] if k else -np.ones(1, np.int64), O.dequantize_swa(rc, rs))
+        assert Hh.attn_rel_err(np_(out[b]), ref) <= Hh.ATTN_TOL, b
 
 
 def test_attention_index_past_len_is_flagged():

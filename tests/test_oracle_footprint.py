@@ -65,3 +65,25 @@ def test_printed_880_and_832_do_not_follow_from_the_formula():
     noscale = csa2.bytes_per_token(main_block=None, idx_block=None)
     assert (with32, noscale) == (850.0, 800.0)
     assert [with32, noscale] != G["not_reproducible"]["printed"]
+
+
+def test_four_layer_store_writes_890_bytes_per_token():
+    """Packing T tokens into the four source layers stores 890 bytes per token, with
+    T/2 entries in each ratio-2 layer and T in the ratio-1 layer ('Le compte par
+    couche', table and eq. 890)."""
+    rng = np.random.default_rng(4)
+    T = 96
+    src = [(rng.standard_normal((T, 512)).astype(np.float32), rng.standard_normal((T, 128)).astype(np.float32))
+           for _ in range(4)]
+    w = [[rng.uniform(0, 1, n).astype(np.float32) for n in (512, 512, 128, 128)] if ratio == 2 else None
+         for _, _, ratio in csa2.SOURCE_LAYERS]
+    rows = csa2.store_entries(src, weights=w)
+    stored = sum(sum(a.nbytes for a in r) for r in rows)
+    assert stored / T == G["bytes_per_token"]["value"]
+    assert [r[0].shape[0] for r in rows] == [T // 2, T // 2, T // 2, T]
+    for (lat, key), (_, _, ratio), ww, r in zip(src, csa2.SOURCE_LAYERS, w, rows):
+        ref = csa2.encode_entries(lat, key, ratio, *(ww or [None] * 4))
+        assert all(np.array_equal(a, b) for a, b in zip(r, ref))
+    # a 1,048,576-token session: 0.87 GiB
+    per_tok = stored / T
+    assert round(1048576 * per_tok / 2 ** 30, 2) == 0.87

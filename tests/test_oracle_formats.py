@@ -62,3 +62,8 @@ def test_ratio2_with_unit_weights_equals_ratio1_of_even_tokens():
     r1 = csa2.encode_entries(lat[0::2], key[0::2], 1)
     for a, b in zip(r2, r1):
         assert np.array_equal(a, b)
+
+
+def test_fp8_window_rows_vs_exact_brute_force():
+    from oracle import csa2
+    P.check_quantize_swa(csa2.quantize_swa, csa2.dequantize_swa)

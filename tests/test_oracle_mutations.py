@@ -150,3 +150,22 @@ def test_reuse_of_the_full_selection_instead_of_the_latest_is_caught():
         return ([o2 if L["mode"] == csa2.REUSE else o for L, o, o2 in zip(layers, outs, outs2)],
                 [i2 if L["mode"] == csa2.REUSE else i for L, i, i2 in zip(layers, idxs, idxs2)])
     _fails(_modes, reuse_full)
+
+
+def test_fp8_window_exponent_or_block_mistakes_are_caught(monkeypatch):
+    real = csa2.quantize_swa
+
+    def emax7(x):  # the scale exponent off by one
+        x = np.asarray(x, np.float32)
+        c, s = real(x * np.float32(2.0))
+        return c, (s.astype(np.int64) - 1).astype(np.uint8)
+    _fails(P.check_quantize_swa, emax7, csa2.dequantize_swa)
+
+    def block32(x):  # one scale per 32 values
+        x = np.asarray(x, np.float32)
+        n = x.shape[0]
+        b = x.reshape(n, 16, 32)
+        amax = np.repeat(np.abs(b).max(-1, keepdims=True), 32, -1).reshape(n, 512)
+        c, s = real(np.where(np.arange(512) % 16 == 0, amax * np.sign(x + 1e-30), x).astype(np.float32))
+        return c, s
+    _fails(P.check_quantize_swa, block32, csa2.dequantize_swa)
