@@ -112,6 +112,12 @@ __device__ __forceinline__ void pdl_wait_and_release() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
+// The two halves, for a kernel that lets the next one launch only near its end (the
+// streaming scan: a cluster kernel placed next to its last blocks could find no room
+// for its last clusters until its own first ones ended).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint32_t smem_u32addr(const void* p) { return smem_u32(p); }

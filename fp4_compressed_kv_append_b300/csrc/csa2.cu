@@ -236,7 +236,7 @@ bool scan_uses_tcgen05() {
 
 void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t* codes, const uint8_t* scales,
                  int64_t cap, const int32_t* len, const int32_t* cand, int P, float* scores, int batch,
-                 cudaStream_t s) {
+                 cudaStream_t s, int scratch = 0) {
   g_launches += 1;
   CUtensorMap m;
   if (!cand && cap % kTmaRows == 0 && make_codes_map(&m, codes, (int64_t)batch * cap)) {
@@ -249,6 +249,7 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
     t.cap = cap;
     t.len = len;
     t.scores = scores;
+    t.scratch = scratch;
     const int64_t tile_rows = scan_uses_tcgen05() ? kTmaRows : kTmaStageRows;
     t.tiles_per_seq = (cap + tile_rows - 1) / tile_rows;
     t.total_tiles = t.tiles_per_seq * batch;
@@ -275,6 +276,7 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
   a.cand = cand;
   a.P = P;
   a.scores = scores;
+  a.scratch = scratch;
   a.stride = cand ? P : cap;
   a.tiles_per_seq = (a.stride + kScanTile - 1) / kScanTile;
   a.total_tiles = a.tiles_per_seq * batch;
@@ -283,10 +285,10 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
 }
 
 void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,
-                 int32_t* out, int batch, cudaStream_t s) {
+                 int32_t* out, int batch, cudaStream_t s, int discard = 0) {
   ensure_max_smem<k_topk>((int)kTopkSmem);
   launch_k(k_topk, dim3(kTopkCluster, batch), dim3(kTopkThreads), kTopkSmem, s, 0u, scores, stride, n, cand, k,
-           out);
+           out, discard);
   g_launches += 1;
 }
 
@@ -581,8 +583,8 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
   // Top-k of every entry of a cache: scores, then the cluster select
   auto scan_and_select = [&](const void* qi, const float* wi, const uint8_t* kc, const uint8_t* ksc,
                              const csa2_cache_view* c, int32_t* out_idx) {
-    launch_scan(qi, dtype, wi, kc, ksc, c->cap, c->len, nullptr, 0, scores, batch, s);
-    launch_topk(scores, c->len, c->cap, k, nullptr, out_idx, batch, s);
+    launch_scan(qi, dtype, wi, kc, ksc, c->cap, c->len, nullptr, 0, scores, batch, s, 1);
+    launch_topk(scores, c->len, c->cap, k, nullptr, out_idx, batch, s, 1);
   };
 
   const csa2_cache_view* main = nullptr;
@@ -596,11 +598,11 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
       pool = L.pool;
       if (pool > 0) {
         launch_scan(L.q_idx, dtype, L.w_idx, main->idx_codes, main->idx_scales, main->cap, main->len, nullptr, 0,
-                    scores, batch, s);
-        launch_topk(scores, main->len, main->cap, pool, nullptr, pool_idx, batch, s);
+                    scores, batch, s, 1);
+        launch_topk(scores, main->len, main->cap, pool, nullptr, pool_idx, batch, s, 1);
         launch_scan(L.q_idx2, dtype, L.w_idx2, main->idx_codes, main->idx_scales, main->cap, main->len, pool_idx,
-                    pool, pscores, batch, s);
-        launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s);
+                    pool, pscores, batch, s, 1);
+        launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s, 1);
       } else {
         scan_and_select(L.q_idx, L.w_idx, main->idx_codes, main->idx_scales, main, dst);
       }
@@ -609,8 +611,8 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
       const uint8_t* kc = L.own_idx_codes ? L.own_idx_codes : main->idx_codes;
       const uint8_t* ksc = L.own_idx_scales ? L.own_idx_scales : main->idx_scales;
       if (pool > 0) {
-        launch_scan(L.q_idx, dtype, L.w_idx, kc, ksc, main->cap, main->len, pool_idx, pool, pscores, batch, s);
-        launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s);
+        launch_scan(L.q_idx, dtype, L.w_idx, kc, ksc, main->cap, main->len, pool_idx, pool, pscores, batch, s, 1);
+        launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s, 1);
       } else {
         scan_and_select(L.q_idx, L.w_idx, kc, ksc, main, dst);
       }

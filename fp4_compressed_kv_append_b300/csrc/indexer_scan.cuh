@@ -46,6 +46,20 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return p;
 }
 
+// Policy for the scores: a decode step's scores are read back at once by its Top-k,
+// so they are kept in L2 ahead of the streamed keys (evict-last); scores returned to a
+// caller are stored with the normal priority.
+__device__ __forceinline__ uint64_t l2_scores_policy(int scratch) {
+  uint64_t p;
+  if (scratch) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+  else asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void st_score(float* p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+
 // 32-bit read-only load, L2 evict-first (the keys are streamed once).
 __device__ __forceinline__ uint32_t ldg_stream_u32(const void* p, uint64_t pol) {
   uint32_t v;
@@ -103,6 +117,7 @@ struct ScanArgs {
   const int32_t* cand;
   int P;
   float* scores;
+  int scratch;  // the scores are a decode step's scratch (see l2_scores_policy)
   int64_t stride;
   int64_t tiles_per_seq;
   int64_t total_tiles;
@@ -265,6 +280,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan_gather(const S
   const int64_t t_begin = gw * a.total_tiles / nw, t_end = (gw + 1) * a.total_tiles / nw;
   if (t_begin >= t_end) return;
   const uint64_t pol = l2_evict_first_policy();
+  const uint64_t spol = l2_scores_policy(a.scratch);
 
   uint32_t bf[2][4][NPART][2];
   float wsel = 0.f;
@@ -286,7 +302,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) k_indexer_scan_gather(const S
         const int r = t4 ? rh : rl;
         if ((cur.flags >> r) & 1u) {
           const int64_t e = cur.e0 + g + 8 * r;
-          a.scores[(size_t)cur.b * a.stride + e] = ((cur.flags >> (4 + r)) & 1u) ? sc : -INFINITY;
+          st_score(a.scores + (size_t)cur.b * a.stride + e, ((cur.flags >> (4 + r)) & 1u) ? sc : -INFINITY, spol);
         }
       }
     }
@@ -342,6 +358,7 @@ struct TmaScanArgs {
   int64_t cap;
   const int32_t* len;
   float* scores;
+  int scratch;  // the scores are a decode step's scratch (see l2_scores_policy)
   int64_t tiles_per_seq;  // ceil(cap / tile rows): 256-row stages (mma.sync form), 128 (tcgen05 form)
   int64_t total_tiles;
 };
@@ -423,7 +440,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 template <int NPART>
 __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSM)
 k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a) {
-  pdl_wait_and_release();
+  pdl_wait();  // (the next kernel may launch once every thread has released it, at its end)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -493,6 +510,7 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
     const int g = lane >> 2, t4 = lane & 3;
     const int r0 = kTmaWarpRows * warp + g;
     const uint32_t swz = (uint32_t)((g >> 1) & 3);  // the same for every row r0 + 8r
+    const uint64_t spol = l2_scores_policy(a.scratch);
     ScanArgs sa;
     sa.q_idx = a.q_idx;
     sa.q_dtype = a.q_dtype;
@@ -531,13 +549,13 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
 #pragma unroll
           for (int m = 0; m < kTmaWarpM16; ++m) {
             const float sc = scan_m16<NPART>(w[2 * m], w[2 * m + 1], sw[2 * m], sw[2 * m + 1], bf, wsel, t4);
-            if (t4 < 2) sp[16 * m] = sc;
+            if (t4 < 2) st_score(sp + 16 * m, sc, spol);
           }
         } else {  // the last stage of the sequence (and every stage of fp32 queries)
 #pragma unroll
           for (int m = 0; m < kTmaWarpM16; ++m) {
             const float sc = scan_m16<NPART>(w[2 * m], w[2 * m + 1], sw[2 * m], sw[2 * m + 1], bf, wsel, t4);
-            if (t4 < 2 && erow + 16 * m < n_b) sp[16 * m] = sc;
+            if (t4 < 2 && erow + 16 * m < n_b) st_score(sp + 16 * m, sc, spol);
           }
         }
       }
@@ -549,6 +567,10 @@ k_indexer_scan_tma(const __grid_constant__ CUtensorMap tmap, const TmaScanArgs a
       }
     }
   }
+  // one thread of a block releasing the next kernel counts for the whole block, and the
+  // producer warp's idle lanes get here at once: release only when every thread has
+  __syncthreads();
+  pdl_release();
 }
 
 }  // namespace csa2

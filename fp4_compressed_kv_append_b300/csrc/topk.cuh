@@ -15,15 +15,27 @@
 //  0. every block reads its slice once (kept as keys in shared memory when the
 //     slice has at most kRxSliceCap slots, else re-read from global memory by each
 //     pass) and publishes its valid count and key range to every block;
-//  1. if the row has at most k valid slots they are all selected. Otherwise, per
-//     level: each block histograms the keys of the current range [lo, hi] into
+//  1. if the row has at most k valid slots they are all selected. Otherwise:
+//  1a. a bound first: every thread also keeps the largest key it read, and block r
+//     finds lb_r, the lower edge of the bin (one fitted histogram level over its
+//     thread maxima) where m = ceil(k / 8) maxima are reached from the top. The
+//     maxima are keys of distinct slots, so at least 8 m >= k keys of the row are at
+//     or above L = min_r lb_r (lb_r travels with the count and key range). Each
+//     block counts its keys >= L; after one exchange of the counts, when they number
+//     at most kRxListCap (about 600 for k = 512 over 131,072 i.i.d. scores), every
+//     block writes them, in slot order, to block 0's list at the offset the earlier
+//     blocks' counts give. Block 0's first four warps finish (rx_finish_small): the
+//     k-th key from one fitted histogram of the list and a rank inside its bin, then
+//     the list walked in slot order gives the output. Otherwise (heavy ties,
+//     say) the levels below run instead;
+//  1b. per level: each block histograms the keys of the current range [lo, hi] into
 //     kRxBins bins of width 2^shift (the smallest width that covers the range, so
 //     the bins follow the occupied keys); block r sums bins [256 r, 256 r + 256)
 //     over the cluster (distributed shared memory) and publishes the segment
 //     total; every block then finds the segment, and inside it the bin, where the
 //     count from the top reaches the wanted rank. That bin is the next range; the
 //     search ends at a bin of one key T (or early, at a bin taken whole);
-//  1b. as soon as the keys at or above the chosen bin number at most kRxListCap
+//     as soon as the keys at or above the chosen bin number at most kRxListCap
 //     (usually after the first level), every block appends those keys, in slot
 //     order, to block 0's list (one remote atomic reserves its run) and block 0
 //     finishes alone: block-local histogram levels over the list give T, and the
@@ -59,9 +71,14 @@ struct alignas(16) TopkCtl {
   uint32_t cnt[kTopkCluster];         // valid slots, by block
   uint32_t kmin[kTopkCluster], kmax[kTopkCluster];  // key range of the valid slots, by block
   uint32_t gt[kTopkCluster], eq[kTopkCluster];      // selected counts (key > T, key == T), by block
+  uint32_t lb[kTopkCluster], lbok[kTopkCluster];    // bound of each block's thread maxima, and whether it holds
+  uint32_t lcnt[kTopkCluster];                      // keys at or above the row bound, by block
+  uint32_t fcnt[3][4];                              // block 0's finish: per-warp partials (scan; two bits in flight)
+  uint32_t fsum[4];                                 // block 0's finish: per-warp totals of the output scan
   unsigned long long warp_u64[kTopkWarps];
   uint32_t warp_u32[kTopkWarps];
   uint32_t warp_a[kTopkWarps], warp_b[kTopkWarps];
+  uint32_t warp_c[kTopkWarps], warp_d[kTopkWarps], warp_e[kTopkWarps];
   uint32_t bc[4];
   // block 0 only, written by every block: the gathered list
   uint32_t list_n;                    // entries reserved
@@ -132,29 +149,43 @@ __device__ __forceinline__ unsigned long long block_excl_scan64(unsigned long lo
   return before + x - v;
 }
 
-// Block-wide sum, min and max (every thread gets all three).
-__device__ __forceinline__ void block_sum_min_max(uint32_t& c, uint32_t& mn, uint32_t& mx, TopkCtl& sh) {
+// Block-wide sums of c and cv, and min / max of the keys (mn, mx) and of the
+// thread maxima (tmn, tmx); every thread gets all six.
+__device__ __forceinline__ void block_load_stats(uint32_t& c, uint32_t& mn, uint32_t& mx, uint32_t& cv,
+                                                 uint32_t& tmn, uint32_t& tmx, TopkCtl& sh) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     c += __shfl_xor_sync(0xffffffffu, c, o);
     mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    cv += __shfl_xor_sync(0xffffffffu, cv, o);
+    tmn = min(tmn, __shfl_xor_sync(0xffffffffu, tmn, o));
+    tmx = max(tmx, __shfl_xor_sync(0xffffffffu, tmx, o));
   }
   if (lane == 0) {
     sh.warp_u32[wid] = c;
     sh.warp_a[wid] = mn;
     sh.warp_b[wid] = mx;
+    sh.warp_c[wid] = cv;
+    sh.warp_d[wid] = tmn;
+    sh.warp_e[wid] = tmx;
   }
   __syncthreads();
   c = 0;
   mn = 0xFFFFFFFFu;
   mx = 0;
+  cv = 0;
+  tmn = 0xFFFFFFFFu;
+  tmx = 0;
 #pragma unroll
   for (int w = 0; w < kTopkWarps; ++w) {
     c += sh.warp_u32[w];
     mn = min(mn, sh.warp_a[w]);
     mx = max(mx, sh.warp_b[w]);
+    cv += sh.warp_c[w];
+    tmn = min(tmn, sh.warp_d[w]);
+    tmx = max(tmx, sh.warp_e[w]);
   }
   __syncthreads();
 }
@@ -347,9 +378,174 @@ __device__ void rx_finish_list(const uint32_t* lkey, const uint32_t* lslot, uint
   }
 }
 
+// Block 0 after the bound path's gather, threads 0 .. kFinThreads - 1 only (the other
+// warps have left): the list (keys, slots) holds, in slot order, every key >= lo of
+// the row in n <= kRxListCap entries, all <= hi, and the `need` largest are selected.
+// Thread t keeps list entries [KPT t, KPT t + KPT) in registers.
+//  * the need-th largest key T: one histogram of the list over kRxBins bins fitted to
+//    [lo, hi] finds the bin B where the count from the top reaches need; when B holds
+//    at most 32 keys (the usual case), one warp ranks them against each other and
+//    picks T; otherwise the bits of T below the bin width are found one by one (the
+//    entries of B that match the bits chosen so far and have the next bit set are
+//    counted: if they reach the rank still wanted the bit is 1, else 0);
+//  * every key > T and the first (need - count(key > T)) entries with key T are
+//    written in list order, at offsets from one scan of the counts.
+constexpr int kFinThreads = 128;
+constexpr int kFinWarps = kFinThreads / 32;
+static_assert(kFinWarps == 4 && kRxListCap % kFinThreads == 0 && kRxListCap <= 65535, "finish shape");
+static_assert(kRxBins % kFinThreads == 0, "whole bins per finishing thread");
+
+__device__ __forceinline__ void fin_bar() { asm volatile("bar.sync 1, %0;\n" ::"n"(kFinThreads) : "memory"); }
+
+// Exclusive scan over the kFinThreads finishing threads (slot: 4 words of shared memory).
+__device__ __forceinline__ uint32_t fin_excl_scan(uint32_t v, uint32_t* slot, uint32_t* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) slot[w] = inc;
+  fin_bar();
+  uint32_t ex = inc - v, tot = 0;
+#pragma unroll
+  for (int q = 0; q < kFinWarps; ++q) {
+    ex += q < w ? slot[q] : 0u;
+    tot += slot[q];
+  }
+  *total = tot;
+  return ex;
+}
+
+__device__ void rx_finish_small(const uint32_t* lkey, const uint32_t* lslot, uint32_t n, uint32_t need, uint32_t lo,
+                                uint32_t hi, TopkCtl& sh, int k, const int32_t* crow, int32_t* orow) {
+  constexpr int KPT = kRxListCap / kFinThreads;   // list entries per thread
+  constexpr int BPT = kRxBins / kFinThreads;      // bins per thread, highest first
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const uint32_t base = KPT * tid;
+  uint32_t key[KPT];
+  uint32_t valid = 0;
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) {
+    const bool v = base + e < n;
+    key[e] = v ? lkey[base + e] : 0u;
+    valid |= (v ? 1u : 0u) << e;
+  }
+  // ---- the bin of rank `need`
+  const uint32_t shift = rx_shift(hi - lo);
+  uint32_t* hist = sh.hist[1];
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) hist[BPT * tid + j] = 0;
+  fin_bar();
+#pragma unroll
+  for (int e = 0; e < KPT; ++e)
+    if ((valid >> e) & 1u) atomicAdd(&hist[(key[e] - lo) >> shift], 1u);
+  fin_bar();
+  const int btop = kRxBins - 1 - BPT * tid;
+  uint32_t own = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) own += hist[btop - j];
+  uint32_t tot;
+  const uint32_t above = fin_excl_scan(own, sh.fcnt[0], &tot);
+  if (above < need && above + own >= need) {
+    uint32_t acc = above;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+      const uint32_t h = hist[btop - j];
+      if (acc < need && acc + h >= need) {
+        sh.bc[0] = (uint32_t)(btop - j);
+        sh.bc[1] = acc;
+        sh.bc[2] = h;
+      }
+      acc += h;
+    }
+  }
+  if (tid == 0) sh.bc[3] = 0;  // keys of bin B collected so far
+  fin_bar();
+  const uint32_t B = sh.bc[0], above_b = sh.bc[1], cnt_b = sh.bc[2];
+  const uint32_t blo = lo + (B << shift);
+  const uint32_t r = need - above_b;  // rank wanted inside bin B (1-based)
+  auto in_b = [&](int e) { return ((valid >> e) & 1u) && ((key[e] - lo) >> shift) == B; };
+  uint32_t T;
+  if (above_b + cnt_b == need) {  // bin B is taken whole
+    // every key >= blo: T is the smallest key of B, and all keys equal to it are taken
+    uint32_t m = 0xFFFFFFFFu;
+#pragma unroll
+    for (int e = 0; e < KPT; ++e)
+      if (in_b(e)) m = min(m, key[e]);
+    m = __reduce_min_sync(0xffffffffu, m);
+    if (lane == 0) sh.fcnt[1][w] = m;
+    fin_bar();
+    T = min(min(sh.fcnt[1][0], sh.fcnt[1][1]), min(sh.fcnt[1][2], sh.fcnt[1][3]));
+  } else if (cnt_b <= 32) {
+    // collect the keys of B and rank them in one warp
+    uint32_t* bk = sh.hist[0];  // (free in this path)
+#pragma unroll
+    for (int e = 0; e < KPT; ++e)
+      if (in_b(e)) bk[atomicAdd(&sh.bc[3], 1u)] = key[e];
+    fin_bar();
+    if (w == 0) {
+      const uint32_t mine = lane < (int)cnt_b ? bk[lane] : 0u;
+      uint32_t gt = 0, ge = 0;
+      for (int j = 0; j < (int)cnt_b; ++j) {
+        const uint32_t o = __shfl_sync(0xffffffffu, mine, j);
+        gt += o > mine ? 1u : 0u;
+        ge += o >= mine ? 1u : 0u;
+      }
+      if (lane < (int)cnt_b && gt < r && r <= ge) sh.bc[3] = mine;  // every such lane holds the same key
+    }
+    fin_bar();
+    T = sh.bc[3];
+  } else {
+    // bit by bit over the offsets key - blo (< 2^shift) of the entries of B
+    uint32_t mask = 0, prefix = 0, rem = r;
+    for (int bit = (int)shift - 1; bit >= 0; --bit) {
+      const uint32_t m2 = mask | (1u << bit), p2 = prefix | (1u << bit);
+      uint32_t c = 0;
+#pragma unroll
+      for (int e = 0; e < KPT; ++e) c += (in_b(e) && ((key[e] - blo) & m2) == p2) ? 1u : 0u;
+      c = __reduce_add_sync(0xffffffffu, c);
+      if (lane == 0) sh.fcnt[1 + (bit & 1)][w] = c;
+      fin_bar();
+      c = sh.fcnt[1 + (bit & 1)][0] + sh.fcnt[1 + (bit & 1)][1] + sh.fcnt[1 + (bit & 1)][2] +
+          sh.fcnt[1 + (bit & 1)][3];
+      if (c >= rem) prefix = p2;
+      else rem -= c;
+      mask = m2;
+    }
+    T = blo + prefix;
+  }
+  // ---- ordered output: (count > T) << 16 | (count == T) per thread, scanned
+  uint32_t gt = 0, eq = 0;
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) {
+    if ((valid >> e) & 1u) {
+      gt += key[e] > T ? 1u : 0u;
+      eq += key[e] == T ? 1u : 0u;
+    }
+  }
+  uint32_t both;
+  const uint32_t ex = fin_excl_scan((gt << 16) | eq, sh.fsum, &both);
+  const uint32_t take_eq = need - (both >> 16);  // ties taken, in list order
+  uint32_t eqi = ex & 0xFFFFu;
+  uint32_t pos = (ex >> 16) + min(take_eq, eqi);
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) {
+    if ((valid >> e) & 1u) {
+      bool take = key[e] > T;
+      if (key[e] == T) take = eqi++ < take_eq;
+      if (take && pos < (uint32_t)k) {
+        const uint32_t sl = lslot[base + e];
+        orow[pos++] = crow ? __ldg(crow + sl) : (int32_t)sl;
+      }
+    }
+  }
+}
+
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 2)
 k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ nvec,
-       const int32_t* __restrict__ cand, int k, int32_t* __restrict__ out) {
+       const int32_t* __restrict__ cand, int k, int32_t* __restrict__ out, int discard) {
   pdl_wait_and_release();
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
@@ -389,8 +585,9 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
   R.vec = (((uintptr_t)row | (uintptr_t)crow) & 15u) == 0;
   R.kept = slen <= kRxSliceCap;
 
-  // ---- 0. read the slice (kept in shared memory when it fits), count, key range
-  uint32_t c = 0, mn = 0xFFFFFFFFu, mx = 0;
+  // ---- 0. read the slice (kept in shared memory when it fits), count, key range;
+  // every thread also keeps the largest key it read (tkey; tv: it read a valid slot)
+  uint32_t c = 0, mn = 0xFFFFFFFFu, mx = 0, tkey = 0, tv = 0;
   if (R.kept && R.vec && !crow) {
     // plain scores: the block reads the slice in coalesced 16-byte chunks (chunk g
     // by thread g % threads) and files chunk g under its run owner g / cpr
@@ -422,6 +619,8 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
             ++c;
             mn = min(mn, kk[u]);
             mx = max(mx, kk[u]);
+            tkey = max(tkey, kk[u]);
+            tv = 1;
           } else {
             kk[u] = 0u;
           }
@@ -449,6 +648,8 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
           ++c;
           mn = min(mn, kk[u]);
           mx = max(mx, kk[u]);
+          tkey = max(tkey, kk[u]);
+          tv = 1;
         }
       }
       if (s0 < R.s_end) keys4[rx_kidx(j, tid)] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
@@ -459,10 +660,59 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
       ++c;
       mn = min(mn, key);
       mx = max(mx, key);
+      tkey = max(tkey, key);
+      tv = 1;
     });
   }
-  for (int j = tid; j < kRxBins; j += kTopkThreads) sh.hist[0][j] = 0;
-  block_sum_min_max(c, mn, mx, sh);  // (its barriers also order the kept keys and hist[0])
+  for (int j = tid; j < kRxBins; j += kTopkThreads) {
+    sh.hist[0][j] = 0;
+    sh.hist[1][j] = 0;
+  }
+  uint32_t cv = tv, tmn = tv ? tkey : 0xFFFFFFFFu, tmx = tkey;
+  block_load_stats(c, mn, mx, cv, tmn, tmx, sh);  // (its barriers also order the kept keys and hist[])
+  if (discard && R.kept) {
+    // the scores are a decode step's scratch, now held as keys: drop the slice's whole
+    // 128-byte lines from L2 without writing them back (lines shared with a
+    // neighbouring slice stay)
+    const uintptr_t a0 = ((uintptr_t)(row + lo_slot) + 127u) & ~(uintptr_t)127u;
+    const uintptr_t a1 = (uintptr_t)(row + hi_slot) & ~(uintptr_t)127u;
+    for (uintptr_t ad = a0 + 128u * (uintptr_t)tid; ad < a1; ad += 128u * kTopkThreads)
+      asm volatile("discard.global.L2 [%0], 128;\n" ::"l"(ad) : "memory");
+  }
+
+  // ---- 0b. a lower bound of the row's k-th key. The threads' largest keys sit in
+  // distinct slots, so if every block has m = ceil(k / clusters) thread maxima at or
+  // above its bound lb, at least k keys of the row are at or above the smallest lb.
+  // lb: the lower edge of the bin (one fitted histogram level over the block's thread
+  // maxima) where the count from the top reaches m.
+  const uint32_t m_th = ((uint32_t)k + kTopkCluster - 1) / kTopkCluster;
+  // (R.kept can differ between blocks; every block must hold for the bound to be used)
+  const bool lb_ok = R.kept && cv >= m_th && (uint32_t)k <= kRxListCap;
+  uint32_t lb = 0;
+  if (lb_ok) {
+    const uint32_t tshift = rx_shift(tmx - tmn);
+    if (tv) atomicAdd(&sh.hist[1][(tkey - tmn) >> tshift], 1u);
+    __syncthreads();
+    constexpr int BPT = kRxBins / kTopkThreads;  // bins per thread, highest first
+    const int btop = kRxBins - 1 - BPT * tid;
+    uint32_t own = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) own += sh.hist[1][btop - j];
+    uint32_t tot;
+    const uint32_t above = block_excl_scan(own, sh, &tot);
+    if (above < m_th && above + own >= m_th) {
+      uint32_t acc = above;
+#pragma unroll
+      for (int j = 0; j < BPT; ++j) {
+        const uint32_t h = sh.hist[1][btop - j];
+        if (acc < m_th && acc + h >= m_th) sh.bc[0] = (uint32_t)(btop - j);
+        acc += h;
+      }
+    }
+    __syncthreads();
+    lb = tmn + (sh.bc[0] << tshift);
+    for (int j = tid; j < kRxBins; j += kTopkThreads) sh.hist[1][j] = 0;  // (levels start from zeroed bins)
+  }
 
   cluster_wait();
   if (tid < kTopkCluster) {
@@ -470,19 +720,63 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
     dst.cnt[rank] = c;
     dst.kmin[rank] = mn;
     dst.kmax[rank] = mx;
+    dst.lb[rank] = lb;
+    dst.lbok[rank] = lb_ok ? 1u : 0u;
   }
   cluster.sync();
-  uint32_t V = 0, klo = 0xFFFFFFFFu, khi = 0;
+  uint32_t V = 0, klo = 0xFFFFFFFFu, khi = 0, L = 0xFFFFFFFFu;
+  bool bound = true;
   for (int q = 0; q < kTopkCluster; ++q) {
     V += sh.cnt[q];
     if (sh.cnt[q]) {
       klo = min(klo, sh.kmin[q]);
       khi = max(khi, sh.kmax[q]);
     }
+    bound = bound && sh.lbok[q] != 0;
+    L = min(L, sh.lb[q]);
   }
   // ---- 1. the threshold: select key > Tc, and the first take_eq slots with key == Tc
   long long Tc = -1;       // every valid key is > -1
   uint32_t take_eq = 0;
+  if (V > (uint32_t)k && bound) {
+    // ---- 1a. every key >= L goes to block 0's list when they number at most
+    // kRxListCap (one count exchange, then each block writes its run, in slot order, at
+    // the offset the earlier blocks' counts give); block 0 finishes alone
+    uint32_t own = 0;
+    unsigned long long qmask = 0;  // the run's slots that qualify
+    rx_visit(R, keys4, vbits, [&](uint32_t sl, uint32_t key) {
+      if (key >= L) {
+        ++own;
+        qmask |= 1ull << (sl - R.s_begin);
+      }
+    });
+    uint32_t cnt_r;
+    const uint32_t at0 = block_excl_scan(own, sh, &cnt_r);
+    if (tid < kTopkCluster) cluster.map_shared_rank(&sh, (unsigned)tid)->lcnt[rank] = cnt_r;
+    cluster.sync();  // every block's count is known everywhere
+    uint32_t total = 0, off = 0;
+    for (int q = 0; q < kTopkCluster; ++q) {
+      off += q < (int)rank ? sh.lcnt[q] : 0u;
+      total += sh.lcnt[q];
+    }
+    if (total <= kRxListCap) {
+      uint32_t at = off + at0;
+      uint32_t* lkey0 = cluster.map_shared_rank(lkey, 0u);
+      uint32_t* lslot0 = cluster.map_shared_rank(lslot, 0u);
+      while (qmask) {
+        const int bi = __ffsll((long long)qmask) - 1;
+        qmask &= qmask - 1;
+        lkey0[at] = reinterpret_cast<const uint32_t*>(keys4 + rx_kidx((uint32_t)bi >> 2, tid))[bi & 3];
+        lslot0[at] = R.s_begin + (uint32_t)bi;
+        ++at;
+      }
+      cluster.sync();  // the last cluster barrier: only block 0's first four warps go on
+      if (rank != 0 || tid >= kFinThreads) return;
+      rx_finish_small(lkey, lslot, total, (uint32_t)k, L, khi, sh, k, crow, orow);
+      return;  // exactly k selected: no padding
+    }
+    // too many keys reach the bound (heavy ties, say): the histogram levels below
+  }
   if (V > (uint32_t)k) {
     uint32_t need = (uint32_t)k;  // still to select inside [klo, khi]
     for (int level = 0;; ++level) {
