@@ -284,11 +284,25 @@ void launch_scan(const void* q_idx, csa2_dtype dt, const float* w, const uint8_t
   else launch_scan_gather<1>(a, s);
 }
 
+template <int THREADS, int CLUSTER>
+void launch_topk_shape(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,
+                       int32_t* out, int batch, cudaStream_t s, int discard) {
+  constexpr size_t smem = topk_smem<THREADS, CLUSTER>();
+  ensure_max_smem<k_topk<THREADS, CLUSTER>>((int)smem);
+  launch_k(k_topk<THREADS, CLUSTER>, dim3(CLUSTER, batch), dim3(THREADS), smem, s, 0u, scores, stride, n, cand, k,
+           out, discard);
+}
+
+// One cluster per row: four blocks when their slices (stride / 4) fit in shared
+// memory, which keeps rows of up to 73,728 slots in a single wave of 71 clusters on
+// B300 (64-row batches); eight otherwise (rows up to 147,456 slots kept; longer rows
+// are re-read from global memory by each pass).
 void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,
                  int32_t* out, int batch, cudaStream_t s, int discard = 0) {
-  ensure_max_smem<k_topk>((int)kTopkSmem);
-  launch_k(k_topk, dim3(kTopkCluster, batch), dim3(kTopkThreads), kTopkSmem, s, 0u, scores, stride, n, cand, k,
-           out, discard);
+  if ((uint64_t)stride <= 4ull * TopkCtl<512, 4>::kSliceCap)
+    launch_topk_shape<512, 4>(scores, n, stride, k, cand, out, batch, s, discard);
+  else
+    launch_topk_shape<512, 8>(scores, n, stride, k, cand, out, batch, s, discard);
   g_launches += 1;
 }
 

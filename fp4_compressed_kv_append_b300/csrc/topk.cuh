@@ -21,13 +21,13 @@
 //     thread maxima) where m = ceil(k / 8) maxima are reached from the top. The
 //     maxima are keys of distinct slots, so at least 8 m >= k keys of the row are at
 //     or above L = min_r lb_r (lb_r travels with the count and key range). Each
-//     block counts its keys >= L; after one exchange of the counts, when they number
-//     at most kRxListCap (about 600 for k = 512 over 131,072 i.i.d. scores), every
-//     block writes them, in slot order, to block 0's list at the offset the earlier
-//     blocks' counts give. Block 0's first four warps finish (rx_finish_small): the
-//     k-th key from one fitted histogram of the list and a rank inside its bin, then
-//     the list walked in slot order gives the output. Otherwise (heavy ties,
-//     say) the levels below run instead;
+//     block writes its keys >= L, in slot order, into its own region of block 0's
+//     list (kRxListCap / 8 entries; about 75 each for k = 512 over 131,072 i.i.d.
+//     scores) and its count to every block. After that one barrier, if every region
+//     held its keys, block 0's first four warps line the regions up and finish
+//     (rx_finish_small): the k-th key from one fitted histogram of the list and a
+//     rank inside its bin, then the list walked in slot order gives the output.
+//     Otherwise (heavy ties, say) the levels below run instead;
 //  1b. per level: each block histograms the keys of the current range [lo, hi] into
 //     kRxBins bins of width 2^shift (the smallest width that covers the range, so
 //     the bins follow the occupied keys); block r sums bins [256 r, 256 r + 256)
@@ -54,48 +54,66 @@
 
 namespace csa2 {
 
-constexpr int kTopkThreads = 512;
-constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkCluster = 8;
 constexpr int kRxBins = 2048;                          // bins per level
-constexpr int kRxSegBins = kRxBins / kTopkCluster;     // 256 bins summed by each block
 constexpr uint32_t kRxRunCap = 36;                     // slots per thread kept in shared memory
-constexpr uint32_t kRxSliceCap = kRxRunCap * kTopkThreads;  // 18,432 per block: rows up to 147,456
 constexpr uint32_t kRxListCap = 2048;                  // keys block 0 finishes alone
-static_assert(kRxSegBins <= kTopkThreads, "one thread per segment bin");
 static_assert(kRxRunCap % 4 == 0 && kRxRunCap < 64, "runs of whole chunks; valid bits in one 64-bit word");
 
+// Control block of one cluster shape: THREADS threads per block, CLUSTER blocks per
+// row. The shape's constants live here so every helper that takes the control block
+// knows them.
+template <int THREADS, int CLUSTER>
 struct alignas(16) TopkCtl {
+  static constexpr int kThreads = THREADS;
+  static constexpr int kWarps = THREADS / 32;
+  static constexpr int kCluster = CLUSTER;
+  static constexpr int kSegBins = kRxBins / CLUSTER;            // bins summed by each block
+  static constexpr uint32_t kSliceCap = kRxRunCap * THREADS;    // slots a block keeps
+  static_assert(kSegBins <= THREADS, "one thread per segment bin");
+
   uint32_t hist[2][kRxBins];          // this block's histogram; levels alternate
-  uint32_t seg[2][kTopkCluster];      // segment totals of the cluster histogram, by block
-  uint32_t cnt[kTopkCluster];         // valid slots, by block
-  uint32_t kmin[kTopkCluster], kmax[kTopkCluster];  // key range of the valid slots, by block
-  uint32_t gt[kTopkCluster], eq[kTopkCluster];      // selected counts (key > T, key == T), by block
-  uint32_t lb[kTopkCluster], lbok[kTopkCluster];    // bound of each block's thread maxima, and whether it holds
-  uint32_t lcnt[kTopkCluster];                      // keys at or above the row bound, by block
-  uint32_t fcnt[3][4];                              // block 0's finish: per-warp partials (scan; two bits in flight)
-  uint32_t fsum[4];                                 // block 0's finish: per-warp totals of the output scan
-  unsigned long long warp_u64[kTopkWarps];
-  uint32_t warp_u32[kTopkWarps];
-  uint32_t warp_a[kTopkWarps], warp_b[kTopkWarps];
-  uint32_t warp_c[kTopkWarps], warp_d[kTopkWarps], warp_e[kTopkWarps];
+  uint32_t seg[2][CLUSTER];           // segment totals of the cluster histogram, by block
+  uint32_t cnt[CLUSTER];              // valid slots, by block
+  uint32_t kmin[CLUSTER], kmax[CLUSTER];  // key range of the valid slots, by block
+  uint32_t gt[CLUSTER], eq[CLUSTER];      // selected counts (key > T, key == T), by block
+  uint32_t lb[CLUSTER], lbok[CLUSTER];    // bound of each block's thread maxima, and whether it holds
+  uint32_t lcnt[CLUSTER];                 // keys at or above the row bound, by block
+  uint32_t fcnt[3][4];                    // block 0's finish: per-warp partials (scan; two bits in flight)
+  uint32_t fsum[4];                       // block 0's finish: per-warp totals of the output scan
+  unsigned long long warp_u64[THREADS / 32];
+  uint32_t warp_u32[THREADS / 32];
+  uint32_t warp_a[THREADS / 32], warp_b[THREADS / 32];
+  uint32_t warp_c[THREADS / 32], warp_d[THREADS / 32], warp_e[THREADS / 32];
   uint32_t bc[4];
   // block 0 only, written by every block: the gathered list
-  uint32_t list_n;                    // entries reserved
-  uint32_t seg_off[kTopkCluster], seg_cnt[kTopkCluster];  // block r's run of the list
+  uint32_t list_n;                        // entries reserved
+  uint32_t seg_off[CLUSTER], seg_cnt[CLUSTER];  // block r's run of the list
 };
 
-static_assert(sizeof(TopkCtl) % 16 == 0, "the kept keys after the control block are read 16 bytes at a time");
-
-// Shared memory: the control block, the kept keys (kRxSliceCap), their valid bits
-// (one 64-bit word per thread) and block 0's gathered list (keys, slots): 109 KB,
-// two blocks per SM.
-constexpr size_t kTopkSmem = sizeof(TopkCtl) + 4u * kRxSliceCap + 8u * kTopkThreads + 8u * kRxListCap;
+// Shared memory of a shape: the control block, the kept keys (kSliceCap), their
+// valid bits (one 64-bit word per thread) and block 0's gathered list (keys, slots):
+// 109 KB for 512 threads (two blocks per SM).
+template <int THREADS, int CLUSTER>
+constexpr size_t topk_smem() {
+  static_assert(sizeof(TopkCtl<THREADS, CLUSTER>) % 16 == 0,
+                "the kept keys after the control block are read 16 bytes at a time");
+  return sizeof(TopkCtl<THREADS, CLUSTER>) + 4u * kRxRunCap * THREADS + 8u * THREADS + 8u * kRxListCap;
+}
 
 // Kept keys: chunk j (4 keys) of thread t's run. The XOR keeps both the run
 // owner's 16-byte reads (fixed j) and the coalesced filing (8 consecutive chunks
 // of a run per 8 lanes) free of bank conflicts.
-__device__ __forceinline__ uint32_t rx_kidx(uint32_t j, uint32_t t) { return j * kTopkThreads + (t ^ j); }
+template <int THREADS>
+__device__ __forceinline__ uint32_t rx_kidx(uint32_t j, uint32_t t) { return j * THREADS + (t ^ j); }
+
+// The shape's constants under the names the code below uses.
+#define CSA2_TOPK_SHAPE(Ctl)                                   \
+  constexpr int kTopkThreads = Ctl::kThreads;                  \
+  constexpr int kTopkWarps = Ctl::kWarps;                      \
+  constexpr int kTopkCluster = Ctl::kCluster;                  \
+  constexpr int kRxSegBins = Ctl::kSegBins;                    \
+  constexpr uint32_t kRxSliceCap = Ctl::kSliceCap;             \
+  (void)kTopkThreads; (void)kTopkWarps; (void)kTopkCluster; (void)kRxSegBins; (void)kRxSliceCap
 
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
@@ -103,7 +121,9 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory"); }
 
 // Exclusive scan over the block of one value per thread; *total gets the sum.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, TopkCtl& sh, uint32_t* total) {
+template <class Ctl>
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Ctl& sh, uint32_t* total) {
+  CSA2_TOPK_SHAPE(Ctl);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   uint32_t x = v;
 #pragma unroll
@@ -126,8 +146,10 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, TopkCtl& sh, uin
 }
 
 // The same for 64-bit values (two 32-bit counts packed high:low).
-__device__ __forceinline__ unsigned long long block_excl_scan64(unsigned long long v, TopkCtl& sh,
+template <class Ctl>
+__device__ __forceinline__ unsigned long long block_excl_scan64(unsigned long long v, Ctl& sh,
                                                                 unsigned long long* total) {
+  CSA2_TOPK_SHAPE(Ctl);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   unsigned long long x = v;
 #pragma unroll
@@ -151,8 +173,10 @@ __device__ __forceinline__ unsigned long long block_excl_scan64(unsigned long lo
 
 // Block-wide sums of c and cv, and min / max of the keys (mn, mx) and of the
 // thread maxima (tmn, tmx); every thread gets all six.
+template <class Ctl>
 __device__ __forceinline__ void block_load_stats(uint32_t& c, uint32_t& mn, uint32_t& mx, uint32_t& cv,
-                                                 uint32_t& tmn, uint32_t& tmx, TopkCtl& sh) {
+                                                 uint32_t& tmn, uint32_t& tmx, Ctl& sh) {
+  CSA2_TOPK_SHAPE(Ctl);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
@@ -221,7 +245,7 @@ __device__ __forceinline__ void rx_load4(const RxRow& R, uint32_t s0, float (&x)
 }
 
 // f(slot, key) for every valid slot of the thread's run, in slot order.
-template <class F>
+template <int kTopkThreads, class F>
 __device__ __forceinline__ void rx_visit(const RxRow& R, const uint4* keys4, const unsigned long long* vbits,
                                          F&& f) {
   if (R.kept) {
@@ -231,7 +255,7 @@ __device__ __forceinline__ void rx_visit(const RxRow& R, const uint4* keys4, con
 #pragma unroll
       for (uint32_t j = 0; j < kRxRunCap / 4; ++j) {
         if (4 * j < L) {
-          const uint4 k4 = keys4[rx_kidx(j, threadIdx.x)];
+          const uint4 k4 = keys4[rx_kidx<kTopkThreads>(j, threadIdx.x)];
           f(R.s_begin + 4 * j, k4.x);
           f(R.s_begin + 4 * j + 1, k4.y);
           f(R.s_begin + 4 * j + 2, k4.z);
@@ -244,7 +268,7 @@ __device__ __forceinline__ void rx_visit(const RxRow& R, const uint4* keys4, con
     for (uint32_t j = 0; j < kRxRunCap / 4; ++j) {
       const uint32_t s0 = R.s_begin + 4 * j;
       if (s0 >= R.s_end) break;
-      const uint4 k4 = keys4[rx_kidx(j, threadIdx.x)];
+      const uint4 k4 = keys4[rx_kidx<kTopkThreads>(j, threadIdx.x)];
       const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
       for (int u = 0; u < 4; ++u)
@@ -274,8 +298,10 @@ __device__ __forceinline__ uint32_t rx_shift(uint32_t span) {
 // block-local histogram levels. Returns the tie key T in *T and how many keys
 // equal to T are selected in *take_eq; or *T = bin start - 1 and *take_eq = 0 when
 // a bin is taken whole.
+template <class Ctl>
 __device__ void rx_list_select(const uint32_t* lkey, uint32_t c, uint32_t need, uint32_t lo, uint32_t hi,
-                               TopkCtl& sh, long long* T, uint32_t* take_eq) {
+                               Ctl& sh, long long* T, uint32_t* take_eq) {
+  CSA2_TOPK_SHAPE(Ctl);
   const int tid = threadIdx.x;
   constexpr int BPT = kRxBins / kTopkThreads;  // bins per thread, highest first
   for (;;) {
@@ -330,8 +356,10 @@ __device__ void rx_list_select(const uint32_t* lkey, uint32_t c, uint32_t need, 
 // cl entries, block r's run at seg_off[r] (seg_cnt[r] entries, slot order); keys above
 // hi are selected already, and `need` more come from [lo, hi]. Selects them
 // (rx_list_select) and writes the k positions in ascending slot order.
+template <class Ctl>
 __device__ void rx_finish_list(const uint32_t* lkey, const uint32_t* lslot, uint32_t cl, uint32_t need,
-                               uint32_t lo, uint32_t hi, TopkCtl& sh, int k, const int32_t* crow, int32_t* orow) {
+                               uint32_t lo, uint32_t hi, Ctl& sh, int k, const int32_t* crow, int32_t* orow) {
+  CSA2_TOPK_SHAPE(Ctl);
   const int tid = threadIdx.x;
   long long T;
   uint32_t teq;
@@ -418,8 +446,10 @@ __device__ __forceinline__ uint32_t fin_excl_scan(uint32_t v, uint32_t* slot, ui
   return ex;
 }
 
+template <class Ctl>
 __device__ void rx_finish_small(const uint32_t* lkey, const uint32_t* lslot, uint32_t n, uint32_t need, uint32_t lo,
-                                uint32_t hi, TopkCtl& sh, int k, const int32_t* crow, int32_t* orow) {
+                                uint32_t hi, Ctl& sh, int k, const int32_t* crow, int32_t* orow) {
+  CSA2_TOPK_SHAPE(Ctl);
   constexpr int KPT = kRxListCap / kFinThreads;   // list entries per thread
   constexpr int BPT = kRxBins / kFinThreads;      // bins per thread, highest first
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -543,16 +573,19 @@ __device__ void rx_finish_small(const uint32_t* lkey, const uint32_t* lslot, uin
   }
 }
 
-__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 2)
+template <int THREADS, int CLUSTER>
+__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, THREADS >= 1024 ? 1 : 2)
 k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ nvec,
        const int32_t* __restrict__ cand, int k, int32_t* __restrict__ out, int discard) {
+  using TopkCtlT = TopkCtl<THREADS, CLUSTER>;
+  CSA2_TOPK_SHAPE(TopkCtlT);
   pdl_wait_and_release();
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  TopkCtl& sh = *reinterpret_cast<TopkCtl*>(smem_raw);
-  uint4* keys4 = reinterpret_cast<uint4*>(smem_raw + sizeof(TopkCtl));
-  unsigned long long* vbits = reinterpret_cast<unsigned long long*>(smem_raw + sizeof(TopkCtl) + 4u * kRxSliceCap);
+  TopkCtlT& sh = *reinterpret_cast<TopkCtlT*>(smem_raw);
+  uint4* keys4 = reinterpret_cast<uint4*>(smem_raw + sizeof(TopkCtlT));
+  unsigned long long* vbits = reinterpret_cast<unsigned long long*>(smem_raw + sizeof(TopkCtlT) + 4u * kRxSliceCap);
   uint32_t* lkey = reinterpret_cast<uint32_t*>(vbits + kTopkThreads);  // block 0: the gathered list (keys, then slots)
   uint32_t* lslot = lkey + kRxListCap;
   const uint32_t rank = cluster.block_rank();
@@ -626,7 +659,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
           }
         }
         const uint32_t t = g / cpr, jj = g - t * cpr;
-        keys4[rx_kidx(jj, t)] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+        keys4[rx_kidx<kTopkThreads>(jj, t)] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
       }
     }
     const uint32_t L = R.s_end - R.s_begin;  // valid slots of this thread's run
@@ -652,11 +685,11 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
           tv = 1;
         }
       }
-      if (s0 < R.s_end) keys4[rx_kidx(j, tid)] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+      if (s0 < R.s_end) keys4[rx_kidx<kTopkThreads>(j, tid)] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
     }
     vbits[tid] = vb;
   } else {
-    rx_visit(R, nullptr, nullptr, [&](uint32_t, uint32_t key) {
+    rx_visit<kTopkThreads>(R, nullptr, nullptr, [&](uint32_t, uint32_t key) {
       ++c;
       mn = min(mn, key);
       mx = max(mx, key);
@@ -716,7 +749,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
 
   cluster_wait();
   if (tid < kTopkCluster) {
-    TopkCtl& dst = *cluster.map_shared_rank(&sh, (unsigned)tid);
+    TopkCtlT& dst = *cluster.map_shared_rank(&sh, (unsigned)tid);
     dst.cnt[rank] = c;
     dst.kmin[rank] = mn;
     dst.kmax[rank] = mx;
@@ -739,40 +772,53 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
   long long Tc = -1;       // every valid key is > -1
   uint32_t take_eq = 0;
   if (V > (uint32_t)k && bound) {
-    // ---- 1a. every key >= L goes to block 0's list when they number at most
-    // kRxListCap (one count exchange, then each block writes its run, in slot order, at
-    // the offset the earlier blocks' counts give); block 0 finishes alone
+    // ---- 1a. every key >= L goes to block 0's list: block r writes its keys >= L, in
+    // slot order, into region r of the list (kRxListCap / clusters entries) and its
+    // count to every block; after one barrier every block knows whether all regions
+    // held their keys. If so block 0 lines the regions up in slot order and finishes
+    // alone; otherwise (heavy ties, say) the histogram levels below run instead
+    constexpr uint32_t kSeg = kRxListCap / kTopkCluster;
     uint32_t own = 0;
     unsigned long long qmask = 0;  // the run's slots that qualify
-    rx_visit(R, keys4, vbits, [&](uint32_t sl, uint32_t key) {
+    rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t sl, uint32_t key) {
       if (key >= L) {
         ++own;
         qmask |= 1ull << (sl - R.s_begin);
       }
     });
     uint32_t cnt_r;
-    const uint32_t at0 = block_excl_scan(own, sh, &cnt_r);
-    if (tid < kTopkCluster) cluster.map_shared_rank(&sh, (unsigned)tid)->lcnt[rank] = cnt_r;
-    cluster.sync();  // every block's count is known everywhere
-    uint32_t total = 0, off = 0;
-    for (int q = 0; q < kTopkCluster; ++q) {
-      off += q < (int)rank ? sh.lcnt[q] : 0u;
-      total += sh.lcnt[q];
-    }
-    if (total <= kRxListCap) {
-      uint32_t at = off + at0;
-      uint32_t* lkey0 = cluster.map_shared_rank(lkey, 0u);
-      uint32_t* lslot0 = cluster.map_shared_rank(lslot, 0u);
-      while (qmask) {
+    uint32_t at = block_excl_scan(own, sh, &cnt_r);
+    {
+      uint32_t* lkey0 = cluster.map_shared_rank(lkey, 0u) + kSeg * rank;
+      uint32_t* lslot0 = cluster.map_shared_rank(lslot, 0u) + kSeg * rank;
+      while (qmask && at < kSeg) {
         const int bi = __ffsll((long long)qmask) - 1;
         qmask &= qmask - 1;
-        lkey0[at] = reinterpret_cast<const uint32_t*>(keys4 + rx_kidx((uint32_t)bi >> 2, tid))[bi & 3];
+        lkey0[at] = reinterpret_cast<const uint32_t*>(keys4 + rx_kidx<kTopkThreads>((uint32_t)bi >> 2, tid))[bi & 3];
         lslot0[at] = R.s_begin + (uint32_t)bi;
         ++at;
       }
-      cluster.sync();  // the last cluster barrier: only block 0's first four warps go on
-      if (rank != 0 || tid >= kFinThreads) return;
-      rx_finish_small(lkey, lslot, total, (uint32_t)k, L, khi, sh, k, crow, orow);
+    }
+    if (tid < kTopkCluster) cluster.map_shared_rank(&sh, (unsigned)tid)->lcnt[rank] = cnt_r;
+    cluster.sync();  // counts everywhere; regions complete where they held their keys
+    bool fits = true;
+    for (int q = 0; q < kTopkCluster; ++q) fits = fits && sh.lcnt[q] <= kSeg;
+    if (fits) {
+      if (rank != 0 || tid >= kFinThreads) return;  // only block 0's first four warps go on
+      // line the regions up, in block (= slot) order, over the kept keys (free now)
+      uint32_t* ck = reinterpret_cast<uint32_t*>(keys4);
+      uint32_t* cs = ck + kRxListCap;
+      uint32_t total = 0;
+      for (int q = 0; q < kTopkCluster; ++q) {
+        const uint32_t cq = sh.lcnt[q];
+        for (uint32_t e = tid; e < cq; e += kFinThreads) {
+          ck[total + e] = lkey[kSeg * q + e];
+          cs[total + e] = lslot[kSeg * q + e];
+        }
+        total += cq;
+      }
+      fin_bar();
+      rx_finish_small(ck, cs, total, (uint32_t)k, L, khi, sh, k, crow, orow);
       return;  // exactly k selected: no padding
     }
     // too many keys reach the bound (heavy ties, say): the histogram levels below
@@ -783,7 +829,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
       const int hb = level & 1;
       const uint32_t shift = rx_shift(khi - klo);
       const uint32_t lo = klo, hi = khi;
-      rx_visit(R, keys4, vbits, [&](uint32_t, uint32_t key) {
+      rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t, uint32_t key) {
         if (key - lo <= hi - lo) atomicAdd(&sh.hist[hb][(key - lo) >> shift], 1u);
       });
       cluster.sync();  // every block's histogram of this level is complete
@@ -842,7 +888,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
         // remote atomic and writes it in slot order)
         uint32_t own = 0;
         unsigned long long qmask = 0;  // kept runs: the run's slots that qualify
-        rx_visit(R, keys4, vbits, [&](uint32_t sl, uint32_t key) {
+        rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t sl, uint32_t key) {
           if (key >= blo) {
             ++own;
             if (R.kept) qmask |= 1ull << (sl - R.s_begin);
@@ -851,7 +897,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
         uint32_t cnt_r;
         const uint32_t at0 = block_excl_scan(own, sh, &cnt_r);
         if (tid == 0) {
-          TopkCtl& sh0 = *cluster.map_shared_rank(&sh, 0u);
+          TopkCtlT& sh0 = *cluster.map_shared_rank(&sh, 0u);
           const uint32_t off = atomicAdd(&sh0.list_n, cnt_r);
           sh0.seg_off[rank] = off;
           sh0.seg_cnt[rank] = cnt_r;
@@ -865,12 +911,12 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
           while (qmask) {
             const int bi = __ffsll((long long)qmask) - 1;
             qmask &= qmask - 1;
-            lkey0[at] = reinterpret_cast<const uint32_t*>(keys4 + rx_kidx((uint32_t)bi >> 2, tid))[bi & 3];
+            lkey0[at] = reinterpret_cast<const uint32_t*>(keys4 + rx_kidx<kTopkThreads>((uint32_t)bi >> 2, tid))[bi & 3];
             lslot0[at] = R.s_begin + (uint32_t)bi;
             ++at;
           }
         } else {
-          rx_visit(R, keys4, vbits, [&](uint32_t s, uint32_t key) {
+          rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t s, uint32_t key) {
             if (key >= blo) {
               lkey0[at] = key;
               lslot0[at] = s;
@@ -897,7 +943,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
 
   // ---- 2. ordered output
   uint32_t gt = 0, eq = 0;
-  rx_visit(R, keys4, vbits, [&](uint32_t, uint32_t key) {
+  rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t, uint32_t key) {
     gt += (long long)key > Tc;
     eq += (long long)key == Tc;
   });
@@ -905,7 +951,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
   const unsigned long long ex64 =
       block_excl_scan64(((unsigned long long)gt << 32) | eq, sh, &tot64);
   if (tid < kTopkCluster) {
-    TopkCtl& dst = *cluster.map_shared_rank(&sh, (unsigned)tid);
+    TopkCtlT& dst = *cluster.map_shared_rank(&sh, (unsigned)tid);
     dst.gt[rank] = (uint32_t)(tot64 >> 32);
     dst.eq[rank] = (uint32_t)tot64;
   }
@@ -922,7 +968,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
   long long pos = sel_before + (long long)(ex64 >> 32) +
                   min(max((long long)take_eq - eq_before, 0ll), (long long)(uint32_t)ex64);
   long long eqi = eq_t;
-  rx_visit(R, keys4, vbits, [&](uint32_t s, uint32_t key) {
+  rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t s, uint32_t key) {
     bool take = (long long)key > Tc;
     if ((long long)key == Tc) {
       take = eqi < (long long)take_eq;
