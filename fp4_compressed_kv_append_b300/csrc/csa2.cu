@@ -288,21 +288,34 @@ template <int THREADS, int CLUSTER>
 void launch_topk_shape(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,
                        int32_t* out, int batch, cudaStream_t s, int discard) {
   constexpr size_t smem = topk_smem<THREADS, CLUSTER>();
+  if (CLUSTER > 8) {  // beyond the portable cluster size (set once per device)
+    static std::atomic<int> done[kMaxDevices];
+    const int dev = current_device();
+    if (!done[dev].load(std::memory_order_acquire)) {
+      cudaFuncSetAttribute(k_topk<THREADS, CLUSTER>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      done[dev].store(1, std::memory_order_release);
+    }
+  }
   ensure_max_smem<k_topk<THREADS, CLUSTER>>((int)smem);
   launch_k(k_topk<THREADS, CLUSTER>, dim3(CLUSTER, batch), dim3(THREADS), smem, s, 0u, scores, stride, n, cand, k,
            out, discard);
 }
 
-// One cluster per row: four blocks when their slices (stride / 4) fit in shared
-// memory, which keeps rows of up to 73,728 slots in a single wave of 71 clusters on
-// B300 (64-row batches); eight otherwise (rows up to 147,456 slots kept; longer rows
-// are re-read from global memory by each pass).
+// One cluster per row, every block keeping its slice in shared memory where it can:
+// four 512-thread blocks up to 73,728 slots (71 clusters at once on B300, so a 64-row
+// batch is one wave), eight up to 147,456 (33 at once), sixteen 1,024-thread blocks
+// (one per SM) up to 589,824 (7 at once); beyond that, sixteen 512-thread blocks that
+// re-read their slices from global memory at each pass.
 void launch_topk(const float* scores, const int32_t* n, int64_t stride, int k, const int32_t* cand,
                  int32_t* out, int batch, cudaStream_t s, int discard = 0) {
   if ((uint64_t)stride <= 4ull * TopkCtl<512, 4>::kSliceCap)
     launch_topk_shape<512, 4>(scores, n, stride, k, cand, out, batch, s, discard);
-  else
+  else if ((uint64_t)stride <= 8ull * TopkCtl<512, 8>::kSliceCap)
     launch_topk_shape<512, 8>(scores, n, stride, k, cand, out, batch, s, discard);
+  else if ((uint64_t)stride <= 16ull * TopkCtl<1024, 16>::kSliceCap)
+    launch_topk_shape<1024, 16>(scores, n, stride, k, cand, out, batch, s, discard);
+  else
+    launch_topk_shape<512, 16>(scores, n, stride, k, cand, out, batch, s, discard);
   g_launches += 1;
 }
 

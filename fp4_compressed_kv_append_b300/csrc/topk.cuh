@@ -221,6 +221,7 @@ struct RxRow {
   const float* row;
   const int32_t* crow;
   uint32_t s_begin, s_end;  // this thread's run
+  uint32_t lo, hi;          // the block's slice
   bool kept, vec;
 };
 
@@ -244,8 +245,30 @@ __device__ __forceinline__ void rx_load4(const RxRow& R, uint32_t s0, float (&x)
   }
 }
 
+// Scores and validity of slots s0 .. s0+3 below `end` (s0 < end, s0 a multiple of 4
+// from the slice start).
+__device__ __forceinline__ void rx_load4_to(const RxRow& R, uint32_t s0, uint32_t end, float (&x)[4],
+                                            bool (&ok)[4]) {
+  if (R.vec && s0 + 4 <= end) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(R.row + s0));
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ok[u] = true;
+  } else {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      ok[u] = s0 + u < end;
+      x[u] = ok[u] ? __ldg(R.row + s0 + u) : 0.f;
+    }
+  }
+  if (R.crow) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ok[u] = ok[u] && __ldg(R.crow + s0 + u) >= 0;
+  }
+}
+
 // f(slot, key) for every valid slot of the thread's run, in slot order.
-template <int kTopkThreads, class F>
+template <int kTopkThreads, int kBatch, class F>
 __device__ __forceinline__ void rx_visit(const RxRow& R, const uint4* keys4, const unsigned long long* vbits,
                                          F&& f) {
   if (R.kept) {
@@ -276,14 +299,72 @@ __device__ __forceinline__ void rx_visit(const RxRow& R, const uint4* keys4, con
     }
     return;
   }
+  // re-read from global memory: kBatch chunks of the run in flight before any is used
+  // (shapes whose rows are normally kept use 1, which keeps their registers free)
+  if constexpr (kBatch == 1) {
 #pragma unroll 4
-  for (uint32_t s0 = R.s_begin; s0 < R.s_end; s0 += 4) {
-    float x[4];
-    bool ok[4];
-    rx_load4(R, s0, x, ok);
+    for (uint32_t s0 = R.s_begin; s0 < R.s_end; s0 += 4) {
+      float x[4];
+      bool ok[4];
+      rx_load4(R, s0, x, ok);
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (ok[u]) f(s0 + u, float_order_key(x[u]));
+      for (int u = 0; u < 4; ++u)
+        if (ok[u]) f(s0 + u, float_order_key(x[u]));
+    }
+    return;
+  }
+  for (uint32_t s0 = R.s_begin; s0 < R.s_end; s0 += 4 * kBatch) {
+    float x[kBatch][4];
+    bool ok[kBatch][4];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (s0 + 4 * i < R.s_end) {
+        rx_load4(R, s0 + 4 * i, x[i], ok[i]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ok[i][u] = false;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (ok[i][u]) f(s0 + 4 * i + u, float_order_key(x[i][u]));
+  }
+}
+
+// f(slot, key) for every valid slot of the block's slice, in no particular order. A
+// slice kept in shared memory is visited as by rx_visit; otherwise the block reads it
+// in coalesced 16-byte chunks (chunk g by thread g mod threads), kBatch chunks a
+// thread in flight.
+template <int kTopkThreads, int kBatch, class F>
+__device__ __forceinline__ void rx_visit_any(const RxRow& R, const uint4* keys4, const unsigned long long* vbits,
+                                             F&& f) {
+  if (R.kept) {
+    rx_visit<kTopkThreads, 1>(R, keys4, vbits, f);
+    return;
+  }
+  const uint32_t nch = (R.hi - R.lo + 3) / 4;
+  for (uint32_t g0 = 0; g0 < nch; g0 += kTopkThreads * kBatch) {
+    float x[kBatch][4];
+    bool ok[kBatch][4];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const uint32_t g = g0 + (uint32_t)(i * kTopkThreads) + threadIdx.x;
+      if (g < nch) {
+        rx_load4_to(R, R.lo + 4 * g, R.hi, x[i], ok[i]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ok[i][u] = false;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const uint32_t s0 = R.lo + 4 * (g0 + (uint32_t)(i * kTopkThreads) + threadIdx.x);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (ok[i][u]) f(s0 + u, float_order_key(x[i][u]));
+    }
   }
 }
 
@@ -615,6 +696,8 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
   R.crow = crow;
   R.s_begin = min(lo_slot + run * (uint32_t)tid, hi_slot);
   R.s_end = min(R.s_begin + run, hi_slot);
+  R.lo = lo_slot;
+  R.hi = hi_slot;
   R.vec = (((uintptr_t)row | (uintptr_t)crow) & 15u) == 0;
   R.kept = slen <= kRxSliceCap;
 
@@ -689,7 +772,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
     }
     vbits[tid] = vb;
   } else {
-    rx_visit<kTopkThreads>(R, nullptr, nullptr, [&](uint32_t, uint32_t key) {
+    rx_visit_any<kTopkThreads, (kTopkCluster > 8 && kTopkThreads < 1024 ? 8 : 1)>(R, nullptr, nullptr, [&](uint32_t, uint32_t key) {
       ++c;
       mn = min(mn, key);
       mx = max(mx, key);
@@ -780,7 +863,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
     constexpr uint32_t kSeg = kRxListCap / kTopkCluster;
     uint32_t own = 0;
     unsigned long long qmask = 0;  // the run's slots that qualify
-    rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t sl, uint32_t key) {
+    rx_visit<kTopkThreads, (kTopkCluster > 8 && kTopkThreads < 1024 ? 8 : 1)>(R, keys4, vbits, [&](uint32_t sl, uint32_t key) {
       if (key >= L) {
         ++own;
         qmask |= 1ull << (sl - R.s_begin);
@@ -829,7 +912,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
       const int hb = level & 1;
       const uint32_t shift = rx_shift(khi - klo);
       const uint32_t lo = klo, hi = khi;
-      rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t, uint32_t key) {
+      rx_visit_any<kTopkThreads, (kTopkCluster > 8 && kTopkThreads < 1024 ? 8 : 1)>(R, keys4, vbits, [&](uint32_t, uint32_t key) {
         if (key - lo <= hi - lo) atomicAdd(&sh.hist[hb][(key - lo) >> shift], 1u);
       });
       cluster.sync();  // every block's histogram of this level is complete
@@ -888,7 +971,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
         // remote atomic and writes it in slot order)
         uint32_t own = 0;
         unsigned long long qmask = 0;  // kept runs: the run's slots that qualify
-        rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t sl, uint32_t key) {
+        rx_visit_any<kTopkThreads, (kTopkCluster > 8 && kTopkThreads < 1024 ? 8 : 1)>(R, keys4, vbits, [&](uint32_t sl, uint32_t key) {
           if (key >= blo) {
             ++own;
             if (R.kept) qmask |= 1ull << (sl - R.s_begin);
@@ -916,13 +999,41 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
             ++at;
           }
         } else {
-          rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t s, uint32_t key) {
-            if (key >= blo) {
-              lkey0[at] = key;
-              lslot0[at] = s;
-              ++at;
+          // not kept: in rounds of one chunk per thread (slot order = chunk order =
+          // thread order within a round), each placed by one block scan
+          constexpr uint32_t kQ = 4;  // consecutive chunks a thread per round
+          uint32_t at_run = sh.bc[3];
+          const uint32_t nch = (R.hi - R.lo + 3) / 4;
+          for (uint32_t g0 = 0; g0 < nch; g0 += kTopkThreads * kQ) {
+            float x[kQ][4];
+            bool ok[kQ][4];
+#pragma unroll
+            for (uint32_t i = 0; i < kQ; ++i) {
+              const uint32_t g = g0 + kQ * tid + i;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) ok[i][u] = false;
+              if (g < nch) rx_load4_to(R, R.lo + 4 * g, R.hi, x[i], ok[i]);
             }
-          });
+            uint32_t q = 0;
+#pragma unroll
+            for (uint32_t i = 0; i < kQ; ++i)
+#pragma unroll
+              for (int u = 0; u < 4; ++u) q += (ok[i][u] && float_order_key(x[i][u]) >= blo) ? 1u : 0u;
+            uint32_t rt;
+            uint32_t a = at_run + block_excl_scan(q, sh, &rt);
+#pragma unroll
+            for (uint32_t i = 0; i < kQ; ++i)
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t key = float_order_key(x[i][u]);
+                if (ok[i][u] && key >= blo) {
+                  lkey0[a] = key;
+                  lslot0[a] = R.lo + 4 * (g0 + kQ * tid + i) + (uint32_t)u;
+                  ++a;
+                }
+              }
+            at_run += rt;
+          }
         }
         cluster.sync();  // the last cluster barrier: only block 0 goes on
         if (rank != 0) return;
@@ -943,7 +1054,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
 
   // ---- 2. ordered output
   uint32_t gt = 0, eq = 0;
-  rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t, uint32_t key) {
+  rx_visit_any<kTopkThreads, (kTopkCluster > 8 && kTopkThreads < 1024 ? 8 : 1)>(R, keys4, vbits, [&](uint32_t, uint32_t key) {
     gt += (long long)key > Tc;
     eq += (long long)key == Tc;
   });
@@ -956,19 +1067,76 @@ k_topk(const float* __restrict__ scores, int64_t stride, const int32_t* __restri
     dst.eq[rank] = (uint32_t)tot64;
   }
   cluster.sync();  // the last cluster barrier: from here on, local memory only
-  long long sel_before = 0, eq_before = 0, total = 0;
+  long long sel_before = 0, eq_before = 0, gt_before = 0, total = 0;
   for (int q = 0; q < kTopkCluster; ++q) {
     const long long g = sh.gt[q], e = sh.eq[q];
     const long long te = min(max((long long)take_eq - eq_before, 0ll), e);  // ties block q takes
     if (q < (int)rank) sel_before += g + te;
+    if (q < (int)rank) gt_before += g;
     total += g + te;
     if (q < (int)rank) eq_before += e;
+  }
+  if (!R.kept) {
+    // not kept: in rounds of one chunk per thread, each placed by one block scan; a
+    // taken slot with G keys > T and E ties before it in the row goes to G + min(E,
+    // take_eq)
+    // (kQ consecutive chunks a thread per round: kQ loads in flight, thread order = slot
+    // order)
+    constexpr uint32_t kQ = 4;
+    long long G0 = gt_before, E0 = eq_before;
+    const uint32_t nch = (R.hi - R.lo + 3) / 4;
+    for (uint32_t g0 = 0; g0 < nch; g0 += kTopkThreads * kQ) {
+      float x[kQ][4];
+      bool ok[kQ][4];
+#pragma unroll
+      for (uint32_t i = 0; i < kQ; ++i) {
+        const uint32_t g = g0 + kQ * tid + i;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ok[i][u] = false;
+        if (g < nch) rx_load4_to(R, R.lo + 4 * g, R.hi, x[i], ok[i]);
+      }
+      uint32_t cg = 0, ce = 0;
+#pragma unroll
+      for (uint32_t i = 0; i < kQ; ++i)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (ok[i][u]) {
+            const uint32_t kk = float_order_key(x[i][u]);
+            cg += (long long)kk > Tc ? 1u : 0u;
+            ce += (long long)kk == Tc ? 1u : 0u;
+          }
+        }
+      unsigned long long rt;
+      const unsigned long long rex = block_excl_scan64(((unsigned long long)cg << 32) | ce, sh, &rt);
+      long long G = G0 + (long long)(rex >> 32), E = E0 + (long long)(uint32_t)rex;
+#pragma unroll
+      for (uint32_t i = 0; i < kQ; ++i)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (!ok[i][u]) continue;
+          const uint32_t kk = float_order_key(x[i][u]);
+          const uint32_t sl = R.lo + 4 * (g0 + kQ * tid + i) + (uint32_t)u;
+          if ((long long)kk > Tc) {
+            const long long p = G + min(E, (long long)take_eq);
+            if (p < k) orow[p] = crow ? __ldg(crow + sl) : (int32_t)sl;
+            ++G;
+          } else if ((long long)kk == Tc) {
+            if (E < (long long)take_eq && G + E < k) orow[G + E] = crow ? __ldg(crow + sl) : (int32_t)sl;
+            ++E;
+          }
+        }
+      G0 += (long long)(rt >> 32);
+      E0 += (long long)(uint32_t)rt;
+    }
+    if (rank + 1 == kTopkCluster)
+      for (long long j = total + tid; j < k; j += kTopkThreads) orow[j] = -1;
+    return;
   }
   const long long eq_t = eq_before + (long long)(uint32_t)ex64;  // ties before this thread's run
   long long pos = sel_before + (long long)(ex64 >> 32) +
                   min(max((long long)take_eq - eq_before, 0ll), (long long)(uint32_t)ex64);
   long long eqi = eq_t;
-  rx_visit<kTopkThreads>(R, keys4, vbits, [&](uint32_t s, uint32_t key) {
+  rx_visit<kTopkThreads, (kTopkCluster > 8 && kTopkThreads < 1024 ? 8 : 1)>(R, keys4, vbits, [&](uint32_t s, uint32_t key) {
     bool take = (long long)key > Tc;
     if ((long long)key == Tc) {
       take = eqi < (long long)take_eq;
