@@ -60,7 +60,7 @@ GATHER_BYTES_PER_ENTRY = 288  # latent: 256 B codes + 32 B E4M3 scales
 # reach DRAM during the launch. Traffic grows with the entries scanned, so a launch's
 # traffic is this figure times its entries. None while the kernel has changed since the
 # capture (the line then reports no traffic).
-SCAN_TRAFFIC_PER_ENTRY = 69.95
+SCAN_TRAFFIC_PER_ENTRY = 69.89
 STEPS_PER_GRAPH = 16
 EVENT_STEPS = (7, 15)  # steps of each graph whose scan launches carry CUDA events
 MIN_TIMED_S = 1.0             # shortest timed region
