@@ -40,11 +40,6 @@ constexpr int kScanThreads = kScanWarps * 32;
 constexpr int kScanTile = 32;  // entries per warp iteration
 
 // ------------------------------------------------------------------ PTX helpers
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
-  return p;
-}
 
 // Policy for the scores: a decode step's scores are read back at once by its Top-k,
 // so they are kept in L2 ahead of the streamed keys (evict-last); scores returned to a
@@ -362,80 +357,6 @@ struct TmaScanArgs {
   int64_t tiles_per_seq;  // ceil(cap / tile rows): 256-row stages (mma.sync form), 128 (tcgen05 form)
   int64_t total_tiles;
 };
-
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(bar),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for the phase of the given parity; false after about budget_ns (error
-// recorded) or when another thread of the block has given up (*abort set).
-__device__ __forceinline__ bool mbar_wait_bounded_ns(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                     uint64_t budget_ns) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u) {
-      if (*abort) return false;
-      const uint64_t now = globaltimer_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > budget_ns) {
-        set_dev_error(CSA2_ERR_TIMEOUT);
-        *abort = 1;
-        return false;
-      }
-    }
-  }
-}
-
-// The kernels' waits: about one second.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
-  return mbar_wait_bounded_ns(bar, parity, abort, 1000000000ull);
-}
-
-__device__ __forceinline__ void tma_load_rows(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar,
-                                              uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(pol)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                          uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
-      "%4;\n" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
-      : "memory");
-}
 
 template <int NPART>
 __global__ void __launch_bounds__(kTmaThreads, kTmaBlocksPerSM)

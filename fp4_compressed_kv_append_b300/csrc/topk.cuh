@@ -311,25 +311,25 @@ __device__ __forceinline__ void rx_visit(const RxRow& R, const uint4* keys4, con
       for (int u = 0; u < 4; ++u)
         if (ok[u]) f(s0 + u, float_order_key(x[u]));
     }
-    return;
-  }
-  for (uint32_t s0 = R.s_begin; s0 < R.s_end; s0 += 4 * kBatch) {
-    float x[kBatch][4];
-    bool ok[kBatch][4];
+  } else {
+    for (uint32_t s0 = R.s_begin; s0 < R.s_end; s0 += 4 * kBatch) {
+      float x[kBatch][4];
+      bool ok[kBatch][4];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      if (s0 + 4 * i < R.s_end) {
-        rx_load4(R, s0 + 4 * i, x[i], ok[i]);
-      } else {
+      for (int i = 0; i < kBatch; ++i) {
+        if (s0 + 4 * i < R.s_end) {
+          rx_load4(R, s0 + 4 * i, x[i], ok[i]);
+        } else {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) ok[i][u] = false;
+          for (int u = 0; u < 4; ++u) ok[i][u] = false;
+        }
       }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (ok[i][u]) f(s0 + 4 * i + u, float_order_key(x[i][u]));
     }
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i)
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (ok[i][u]) f(s0 + 4 * i + u, float_order_key(x[i][u]));
   }
 }
 
