@@ -96,13 +96,31 @@ __device__ __forceinline__ void tc_mma_f16_ss(uint32_t d_taddr, uint64_t a_desc,
       : "memory");
 }
 
+// Per-layer operands of one launch: layer blockIdx.z of the grid. Layers launched
+// together share the cache, k, W, H and the query type; each has its own queries,
+// selection, window rows and output.
+constexpr int kAclMaxLayers = 4;
+struct AclLayers {
+  const void* q[kAclMaxLayers];
+  const int32_t* idx[kAclMaxLayers];
+  const uint16_t* swa[kAclMaxLayers];
+  const uint8_t* swa_codes[kAclMaxLayers];
+  const uint8_t* swa_scales[kAclMaxLayers];
+  float* out[kAclMaxLayers];
+};
+
 template <int NPART>
 __global__ void __launch_bounds__(kAclThreads, 1)
-k_sparse_attn_cl(const void* __restrict__ q, int q_dtype, float scale, const uint8_t* __restrict__ lat_codes,
-                 const uint8_t* __restrict__ lat_scales, const int32_t* __restrict__ len, int64_t cap,
-                 const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa,
-                 const uint8_t* __restrict__ swa_codes, const uint8_t* __restrict__ swa_scales, int W, int H,
-                 float* __restrict__ out, int q_early) {
+k_sparse_attn_cl(const __grid_constant__ AclLayers layers, int q_dtype, float scale,
+                 const uint8_t* __restrict__ lat_codes, const uint8_t* __restrict__ lat_scales,
+                 const int32_t* __restrict__ len, int64_t cap, int k, int W, int H, int q_early) {
+  const int li = blockIdx.z;
+  const void* __restrict__ q = layers.q[li];
+  const int32_t* __restrict__ idx = layers.idx[li];
+  const uint16_t* __restrict__ swa = layers.swa[li];
+  const uint8_t* __restrict__ swa_codes = layers.swa_codes[li];
+  const uint8_t* __restrict__ swa_scales = layers.swa_scales[li];
+  float* __restrict__ out = layers.out[li];
   extern __shared__ __align__(1024) unsigned char acl_smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(acl_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

@@ -337,15 +337,33 @@ void launch_attn_t(const void* q, csa2_dtype dt, int H, float scale, const csa2_
            H, out);
 }
 
-// Key-split form: one cluster of ceil((k + W) / 128) blocks per (sequence, 64 heads).
+// One attention layer of a launch: its queries, selection, window rows and output.
+struct AttnLayer {
+  const void* q;
+  const int32_t* idx;
+  Window win;
+  float* out;
+};
+
+// Key-split form: one cluster of ceil((k + W) / 128) blocks per (sequence, 64 heads,
+// layer); the layers of one launch share the cache, k, W, H and the query type.
 template <int NPART>
-void launch_attn_cl(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
-                    int k, const Window& win, float* out, int q_early, cudaStream_t s) {
+void launch_attn_cl(const AttnLayer* L, int nl, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, int k,
+                    int W, int q_early, cudaStream_t s) {
   ensure_max_smem<k_sparse_attn_cl<NPART>>(kAclSmem);
-  const int C = (k + win.W + kAclKeys - 1) / kAclKeys;
-  launch_k(k_sparse_attn_cl<NPART>, dim3((unsigned)(C * (H / kAclHeads)), (unsigned)c.batch), dim3(kAclThreads),
-           kAclSmem, s, (unsigned)C, q, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap, idx, k, win.bf16,
-           win.codes, win.scales, win.W, H, out, q_early);
+  AclLayers t = {};
+  for (int i = 0; i < nl; ++i) {
+    t.q[i] = L[i].q;
+    t.idx[i] = L[i].idx;
+    t.swa[i] = L[i].win.bf16;
+    t.swa_codes[i] = L[i].win.codes;
+    t.swa_scales[i] = L[i].win.scales;
+    t.out[i] = L[i].out;
+  }
+  const int C = (k + W + kAclKeys - 1) / kAclKeys;
+  launch_k(k_sparse_attn_cl<NPART>, dim3((unsigned)(C * (H / kAclHeads)), (unsigned)c.batch, (unsigned)nl),
+           dim3(kAclThreads), kAclSmem, s, (unsigned)C, t, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap,
+           k, W, H, q_early);
 }
 
 // The key-split form covers 64-head groups and up to 1,024 keys per row; the
@@ -360,19 +378,24 @@ bool attn_key_split(int H, int k, int W) {
   return v == 1 && H % kAclHeads == 0 && k + W >= 1 && k + W <= kAclKeys * kAclMaxBlocks;
 }
 
-// q_early: the kernel before this launch on `s` is this library's Top-k, which does
-// not write q (the decode step's Full and Reindex layers); the queries may then be
-// read before waiting for it.
-void launch_attn(const void* q, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, const int32_t* idx,
-                 int k, const Window& win, float* out, cudaStream_t s, int q_early = 0) {
-  if (attn_key_split(H, k, win.W)) {
-    if (dt == CSA2_F32) launch_attn_cl<2>(q, dt, H, scale, c, idx, k, win, out, q_early, s);
-    else launch_attn_cl<1>(q, dt, H, scale, c, idx, k, win, out, q_early, s);
-  } else {
-    if (dt == CSA2_F32) launch_attn_t<2>(q, dt, H, scale, c, idx, k, win, out, s);
-    else launch_attn_t<1>(q, dt, H, scale, c, idx, k, win, out, s);
+// Attention for nl layers (at most kAclMaxLayers, all with the same W) over cache c:
+// one key-split launch covering every layer, or one chunked launch per layer. q_early:
+// the kernel before this launch on `s` is this library's Top-k, which does not write
+// q; the queries may then be read before waiting for it.
+void launch_attn(const AttnLayer* L, int nl, csa2_dtype dt, int H, float scale, const csa2_cache_view& c, int k,
+                 cudaStream_t s, int q_early = 0) {
+  const int W = L[0].win.W;
+  if (attn_key_split(H, k, W)) {
+    if (dt == CSA2_F32) launch_attn_cl<2>(L, nl, dt, H, scale, c, k, W, q_early, s);
+    else launch_attn_cl<1>(L, nl, dt, H, scale, c, k, W, q_early, s);
+    g_launches += 1;
+    return;
   }
-  g_launches += 1;
+  for (int i = 0; i < nl; ++i) {
+    if (dt == CSA2_F32) launch_attn_t<2>(L[i].q, dt, H, scale, c, L[i].idx, k, L[i].win, L[i].out, s);
+    else launch_attn_t<1>(L[i].q, dt, H, scale, c, L[i].idx, k, L[i].win, L[i].out, s);
+    g_launches += 1;
+  }
 }
 
 // One thread waits, with the kernels' bounded wait and the given budget, on an
@@ -469,8 +492,8 @@ csa2_status sparse_latent_attn(const void* q, csa2_dtype q_dtype, int32_t H, flo
   const csa2_status ws = check_window(swa, swa_codes, swa_scales, W);
   if (ws != CSA2_OK) return ws;
   if (!aligned16(q) || !aligned16(out)) return CSA2_ERR_ALIGN;
-  launch_attn(q, q_dtype, H, scale, *cache, idx, k, Window{swa, swa_codes, swa_scales, W}, out,
-              (cudaStream_t)stream);
+  const AttnLayer L{q, idx, Window{swa, swa_codes, swa_scales, W}, out};
+  launch_attn(&L, 1, q_dtype, H, scale, *cache, k, (cudaStream_t)stream);
   return launch_status();
 }
 
@@ -552,8 +575,8 @@ StepLayout step_layout(int32_t batch, int64_t max_entries, int32_t H, int32_t k,
   off += round_up((size_t)batch * (size_t)pool * sizeof(int32_t), 256);
   L.pscores = off;
   off += round_up((size_t)batch * (size_t)pool * sizeof(float), 256);
-  L.sel = off;
-  off += round_up((size_t)batch * (size_t)k * sizeof(int32_t), 256);
+  L.sel = off;  // two selections: a layer's attention can wait for a later layer's
+  off += 2 * round_up((size_t)batch * (size_t)k * sizeof(int32_t), 256);
   L.total = off;
   (void)H;
   (void)W;
@@ -605,7 +628,8 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
   float* scores = reinterpret_cast<float*>(base + SL.scores);
   int32_t* pool_idx = reinterpret_cast<int32_t*>(base + SL.pool);
   float* pscores = reinterpret_cast<float*>(base + SL.pscores);
-  int32_t* sel = reinterpret_cast<int32_t*>(base + SL.sel);
+  int32_t* sel[2] = {reinterpret_cast<int32_t*>(base + SL.sel),
+                     reinterpret_cast<int32_t*>(base + SL.sel + round_up((size_t)batch * (size_t)k * sizeof(int32_t), 256))};
   cudaStream_t s = (cudaStream_t)stream;
   // Top-k of every entry of a cache: scores, then the cluster select
   auto scan_and_select = [&](const void* qi, const float* wi, const uint8_t* kc, const uint8_t* ksc,
@@ -614,34 +638,64 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
     launch_topk(scores, c->len, c->cap, k, nullptr, out_idx, batch, s, 1);
   };
 
+  // Each layer's attention is deferred and launched together with the following
+  // layers' (one launch, one grid layer each) while they share the cache and the
+  // window length: a layer's attention waits at most until a later Top-k would
+  // overwrite the selection it reads, the cache changes, or the group is full.
+  const float scale = 1.0f / sqrtf((float)CSA2_LATENT_DIM);
+  AttnLayer pend[kAclMaxLayers];
+  int np = 0;
+  const csa2_cache_view* pend_cache = nullptr;
+  auto pending_reads = [&](const int32_t* p) {
+    for (int j = 0; j < np; ++j)
+      if (pend[j].idx == p) return true;
+    return false;
+  };
+  auto flush = [&]() {
+    if (np > 0) launch_attn(pend, np, dtype, H, scale, *pend_cache, k, s, 1);
+    np = 0;
+  };
+
   const csa2_cache_view* main = nullptr;
   const int32_t* last = nullptr;
   int pool = 0;
   for (int i = 0; i < n_layers; ++i) {
     const csa2_layer_desc& L = layers[i];
-    int32_t* dst = L.idx_out ? L.idx_out : sel;
-    if (L.mode == CSA2_FULL) {
-      main = L.cache;
-      pool = L.pool;
-      if (pool > 0) {
-        launch_scan(L.q_idx, dtype, L.w_idx, main->idx_codes, main->idx_scales, main->cap, main->len, nullptr, 0,
-                    scores, batch, s, 1);
-        launch_topk(scores, main->len, main->cap, pool, nullptr, pool_idx, batch, s, 1);
-        launch_scan(L.q_idx2, dtype, L.w_idx2, main->idx_codes, main->idx_scales, main->cap, main->len, pool_idx,
-                    pool, pscores, batch, s, 1);
-        launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s, 1);
-      } else {
-        scan_and_select(L.q_idx, L.w_idx, main->idx_codes, main->idx_scales, main, dst);
+    if (L.mode == CSA2_FULL || L.mode == CSA2_REINDEX) {
+      // this layer's selection: its own output array, else a workspace selection that
+      // no deferred attention reads
+      int32_t* dst = L.idx_out;
+      if (!dst) {
+        dst = !pending_reads(sel[0]) ? sel[0] : !pending_reads(sel[1]) ? sel[1] : nullptr;
+        if (!dst) {
+          flush();
+          dst = sel[0];
+        }
+      } else if (pending_reads(dst)) {
+        flush();
       }
-      last = dst;
-    } else if (L.mode == CSA2_REINDEX) {
-      const uint8_t* kc = L.own_idx_codes ? L.own_idx_codes : main->idx_codes;
-      const uint8_t* ksc = L.own_idx_scales ? L.own_idx_scales : main->idx_scales;
-      if (pool > 0) {
-        launch_scan(L.q_idx, dtype, L.w_idx, kc, ksc, main->cap, main->len, pool_idx, pool, pscores, batch, s, 1);
-        launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s, 1);
+      if (L.mode == CSA2_FULL) {
+        main = L.cache;
+        pool = L.pool;
+        if (pool > 0) {
+          launch_scan(L.q_idx, dtype, L.w_idx, main->idx_codes, main->idx_scales, main->cap, main->len, nullptr, 0,
+                      scores, batch, s, 1);
+          launch_topk(scores, main->len, main->cap, pool, nullptr, pool_idx, batch, s, 1);
+          launch_scan(L.q_idx2, dtype, L.w_idx2, main->idx_codes, main->idx_scales, main->cap, main->len, pool_idx,
+                      pool, pscores, batch, s, 1);
+          launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s, 1);
+        } else {
+          scan_and_select(L.q_idx, L.w_idx, main->idx_codes, main->idx_scales, main, dst);
+        }
       } else {
-        scan_and_select(L.q_idx, L.w_idx, kc, ksc, main, dst);
+        const uint8_t* kc = L.own_idx_codes ? L.own_idx_codes : main->idx_codes;
+        const uint8_t* ksc = L.own_idx_scales ? L.own_idx_scales : main->idx_scales;
+        if (pool > 0) {
+          launch_scan(L.q_idx, dtype, L.w_idx, kc, ksc, main->cap, main->len, pool_idx, pool, pscores, batch, s, 1);
+          launch_topk(pscores, nullptr, pool, k, pool_idx, dst, batch, s, 1);
+        } else {
+          scan_and_select(L.q_idx, L.w_idx, kc, ksc, main, dst);
+        }
       }
       last = dst;
     } else if (L.idx_out) {
@@ -649,9 +703,11 @@ csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, in
           cudaSuccess)
         return CSA2_ERR_CUDA;
     }
-    launch_attn(L.q, dtype, H, 1.0f / sqrtf((float)CSA2_LATENT_DIM), *main, last, k,
-                Window{L.swa, L.swa_codes, L.swa_scales, L.W}, L.out, s, L.mode != CSA2_REUSE ? 1 : 0);
+    if (np > 0 && (pend_cache != main || pend[0].win.W != L.W || np == kAclMaxLayers)) flush();
+    pend[np++] = AttnLayer{L.q, last, Window{L.swa, L.swa_codes, L.swa_scales, L.W}, L.out};
+    pend_cache = main;
   }
+  flush();
   return launch_status();
 }
 

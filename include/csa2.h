@@ -259,10 +259,13 @@ typedef struct {
  * The first layer must be FULL. layers is a host array of n_layers descriptors.
  * q, q_idx, q_idx2 share ``dtype``. ws: at least csa2_workspace_size(...) bytes,
  * caller-owned, any contents (every part is written before it is read).
- * Launches only; no host synchronisation inside. The step reads a Full or
- * Reindex layer's q while that layer's Top-k may still run, so q must not
- * overlap any layer's idx_out or the workspace (inputs and outputs are distinct
- * buffers anyway).
+ * Launches only; no host synchronisation inside. The attention of consecutive
+ * layers that share the main KV and the window length W is launched together
+ * (one launch for up to four layers), so a layer's attention may run after later
+ * layers' scans and selections; until then its selection stays in its idx_out or
+ * in one of the workspace's two selections. The step reads a layer's q while the
+ * Top-k before its attention may still run, so q must not overlap any layer's
+ * idx_out or the workspace (inputs and outputs are distinct buffers anyway).
  */
 CSA2_API csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_layers, int32_t batch,
                              int32_t H, int32_t k, csa2_dtype dtype, void* ws, size_t ws_bytes,
@@ -291,13 +294,17 @@ CSA2_API csa2_status csa2_decode_step(const csa2_layer_desc* layers, int32_t n_l
  *     streams, other host threads) race on it and must be serialised by the
  *     caller. Nothing in it needs to start at zero; it keeps the last call's
  *     contents.
+ *   - The array's address is looked up once per device ordinal and kept: after
+ *     cudaDeviceReset (or any other teardown of the device's primary context) in
+ *     the same process that address is stale, so this call is not supported
+ *     after such a reset.
  */
 CSA2_API csa2_status csa2_decode_step_static(const csa2_layer_desc* layers, int32_t n_layers, int32_t batch,
                                              int32_t H, int32_t k, csa2_dtype dtype, csa2_stream_t stream);
 
 /* Scratch bytes of csa2_decode_step for these sizes (max_entries = cap): scores
- * [batch][max_entries] f32, pool positions and scores [batch][pool], selection
- * [batch][k]. */
+ * [batch][max_entries] f32, pool positions and scores [batch][pool], two
+ * selections [batch][k]. */
 CSA2_API size_t csa2_workspace_size(int32_t batch, int64_t max_entries, int32_t H, int32_t k, int32_t pool,
                            int32_t W);
 

@@ -39,9 +39,9 @@ def test_workspace_sizes():
     L = A.lib()
     # the decode step needs the scores, the pool and the selection
     total = L.csa2_workspace_size(32, 131072, 64, 512, 0, 0)
-    assert total >= 32 * 131072 * 4 + 32 * 512 * 4
+    assert total >= 32 * 131072 * 4 + 2 * 32 * 512 * 4  # scores, two selections
     pooled = L.csa2_workspace_size(8, 524288, 64, 512, 16384, 0)
-    assert pooled >= 8 * 524288 * 4 + 2 * 8 * 16384 * 4 + 8 * 512 * 4
+    assert pooled >= 8 * 524288 * 4 + 2 * 8 * 16384 * 4 + 2 * 8 * 512 * 4
 
 
 def _fake_cache(cap=256, batch=2, base=0x10000):
