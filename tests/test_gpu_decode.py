@@ -203,3 +203,29 @@ def test_decode_step_misleading_sample_falls_back_exactly():
         s = O.indexer_scores(np_(q_idx[b]).astype(np.float64), np_(w[b]), keys)
         ref = O.topk_positions(s, k)
         Hh.assert_topk_match(np_(idx[b]), ref, s, where=f"seq {b}")
+
+
+def test_selections_kept_in_the_workspace():
+    """Eight layers (Full, Reindex, Reuse, Reindex, then four Reuse) whose selections
+    stay in the workspace (no idx_out): the deferred attention then uses both
+    workspace selections, is flushed when neither is free (before the second
+    Reindex), and is split at four layers per launch. Every output equals, bit for
+    bit, that of the same step with each selection in its own array, whose outputs
+    are compared with the oracle first."""
+    from fp4_compressed_kv_append_b300 import DecodeStep, Layer
+    modes = (CF.FULL, CF.REINDEX, CF.REUSE, CF.REINDEX, CF.REUSE, CF.REUSE, CF.REUSE, CF.REUSE)
+    c = CF.config(4, B=2, tokens=3000, modes=modes)
+    wl = CF.DecodeWorkload(c)
+    wl()
+    torch.cuda.synchronize()
+    assert Hh.K.sync_status() == 0
+    for b in range(c["B"]):
+        _check_sequence(wl, b)
+    layers = [Layer(L.mode, L.q, torch.full_like(L.out, float("nan")), cache=L.cache, q_idx=L.q_idx, w_idx=L.w_idx,
+                    own_idx_codes=L.own_idx_codes, own_idx_scales=L.own_idx_scales, pool=L.pool, q_idx2=L.q_idx2,
+                    w_idx2=L.w_idx2, swa=L.swa) for L in wl.layers]
+    DecodeStep(layers, CF.TOPK)()
+    torch.cuda.synchronize()
+    assert Hh.K.sync_status() == 0
+    for li, (ref, L) in enumerate(zip(wl.outputs, layers)):
+        assert torch.equal(ref, L.out), f"layer {li}"
