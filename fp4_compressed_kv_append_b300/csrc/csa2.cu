@@ -94,19 +94,25 @@ csa2_status check_cache(const csa2_cache_view* c) {
 }
 
 // ------------------------------------------------------------ launchers (no validation)
+template <auto Kern>
+void ensure_max_smem(int bytes);
+
 void launch_append(const void* lat, const void* ikey, csa2_dtype dt, int T, int ratio, const float* w0l,
                    const float* w1l, const float* w0i, const float* w1i, const csa2_cache_view& c,
                    cudaStream_t s) {
   const int n_new = T / ratio;
   const dim3 grid((n_new + kAppendBlockEntries - 1) / kAppendBlockEntries, c.batch);
-  if (dt == CSA2_F32)
-    launch_k(k_quant_append<float>, grid, dim3(kAppendWarps * 32), 0, s, 0u, (const float*)lat,
-             (const float*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes, c.lat_scales, c.idx_codes,
-             c.idx_scales, c.len, c.cap, n_new);
-  else
-    launch_k(k_quant_append<uint16_t>, grid, dim3(kAppendWarps * 32), 0, s, 0u, (const uint16_t*)lat,
-             (const uint16_t*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes, c.lat_scales, c.idx_codes,
-             c.idx_scales, c.len, c.cap, n_new);
+  if (dt == CSA2_F32) {
+    ensure_max_smem<k_quant_append<float>>((int)append_stage_bytes<float>(2));
+    launch_k(k_quant_append<float>, grid, dim3(kAppendWarps * 32), append_stage_bytes<float>(ratio), s, 0u,
+             (const float*)lat, (const float*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes, c.lat_scales,
+             c.idx_codes, c.idx_scales, c.len, c.cap, n_new);
+  } else {
+    ensure_max_smem<k_quant_append<uint16_t>>((int)append_stage_bytes<uint16_t>(2));
+    launch_k(k_quant_append<uint16_t>, grid, dim3(kAppendWarps * 32), append_stage_bytes<uint16_t>(ratio), s, 0u,
+             (const uint16_t*)lat, (const uint16_t*)ikey, T, ratio, w0l, w1l, w0i, w1i, c.lat_codes, c.lat_scales,
+             c.idx_codes, c.idx_scales, c.len, c.cap, n_new);
+  }
   g_launches += 1;
   if (grid.x > 1) {  // several blocks per sequence: advance len once they are all done
     launch_k(k_bump_len, dim3((c.batch + 255) / 256), dim3(256), 0, s, 0u, c.len, c.batch, c.cap, n_new);
@@ -424,7 +430,11 @@ csa2_status check_window(const uint16_t* swa, const uint8_t* codes, const uint8_
 
 template <typename Tin>
 void launch_store(const StoreArgs& a, int batch, int blocks, cudaStream_t s) {
-  launch_k(k_store_append<Tin>, dim3((unsigned)blocks, (unsigned)batch), dim3(kAppendWarps * 32), 0, s, 0u, a);
+  int rmax = 1;
+  for (int i = 0; i < a.n_layers; ++i) rmax = a.L[i].ratio > rmax ? a.L[i].ratio : rmax;
+  ensure_max_smem<k_store_append<Tin>>((int)append_stage_bytes<Tin>(2));
+  launch_k(k_store_append<Tin>, dim3((unsigned)blocks, (unsigned)batch), dim3(kAppendWarps * 32),
+           append_stage_bytes<Tin>(rmax), s, 0u, a);
   launch_k(k_store_bump, dim3((unsigned)a.n_layers), dim3(256), 0, s, 0u, a, batch);
   g_launches += 2;
 }

@@ -5,6 +5,10 @@
 // (eq. 288) and "Cles d'indexeur" (eq. 68); "compresse le KV-Cache de 4 fois",
 // item 2 (two consecutive positions merged with learned per-channel weights).
 //
+// The block's source tokens (a contiguous run of rows per sequence) are first
+// bulk-copied into shared memory by one thread, so the whole block's input is in
+// flight at once; the warps then pack from shared memory.
+//
 // One warp per output entry. Lane l owns latent channels [16l, 16l+16) -- exactly
 // one E4M3 scale block -- and indexer channels [4l, 4l+4); eight lanes form one
 // 32-channel MXFP4 block. All loads are 16-byte vectors; every lane stores 8 bytes
@@ -78,32 +82,67 @@ __device__ __forceinline__ void e2m1_div16(const float (&x)[16], float s, uint32
   hi = e2m1x8(q + 8);
 }
 
+// Eight / four consecutive source values from shared memory (16- / 8-byte aligned).
+template <typename T>
+__device__ __forceinline__ void load8_shared(const T* p, float (&x)[8]);
+template <>
+__device__ __forceinline__ void load8_shared<float>(const float* p, float (&x)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load8_shared<uint16_t>(const uint16_t* p, float (&x)[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+template <typename T>
+__device__ __forceinline__ void load4_shared(const T* p, float (&x)[4]);
+template <>
+__device__ __forceinline__ void load4_shared<float>(const float* p, float (&x)[4]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+}
+template <>
+__device__ __forceinline__ void load4_shared<uint16_t>(const uint16_t* p, float (&x)[4]) {
+  const uint2 a = *reinterpret_cast<const uint2*>(p);
+  x[0] = __uint_as_float(a.x << 16);
+  x[1] = __uint_as_float(a.x & 0xFFFF0000u);
+  x[2] = __uint_as_float(a.y << 16);
+  x[3] = __uint_as_float(a.y & 0xFFFF0000u);
+}
+
 // One entry: ratio-2 merge (optional), then both packings. Lane l of the warp.
-// Needs only the source token, not the cache position.
+// Needs only the source token, not the cache position. lat / ikey are the block's
+// staged rows in shared memory; tok is the entry's first token among them.
 template <typename Tin>
-__device__ __forceinline__ PackedLane quant_entry(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T,
-                                                  int ratio, const MergeWeights& W, int b, int e, int lane) {
+__device__ __forceinline__ PackedLane quant_entry(const Tin* lat, const Tin* ikey, int tok, int ratio,
+                                                  const MergeWeights& W, int lane) {
   PackedLane P;
-  const size_t tok = (size_t)b * T + (size_t)e * ratio;
 
   // ---- loads: latent (one 16-channel block per lane) and key (4 channels), both tokens
   float x[16], y[16], z[4], zy[4];
   {
-    const Tin* p = lat + tok * 512 + 16 * lane;
+    const Tin* p = lat + (size_t)tok * 512 + 16 * lane;
     float a[8], c[8];
-    load8(p, a);
-    load8(p + 8, c);
+    load8_shared(p, a);
+    load8_shared(p + 8, c);
 #pragma unroll
     for (int i = 0; i < 8; ++i) { x[i] = a[i]; x[8 + i] = c[i]; }
     if (ratio == 2) {
-      load8(p + 512, a);
-      load8(p + 520, c);
+      load8_shared(p + 512, a);
+      load8_shared(p + 520, c);
 #pragma unroll
       for (int i = 0; i < 8; ++i) { y[i] = a[i]; y[8 + i] = c[i]; }
     }
-    const Tin* pk = ikey + tok * 128 + 4 * lane;
-    load4(pk, z);
-    if (ratio == 2) load4(pk + 128, zy);
+    const Tin* pk = ikey + (size_t)tok * 128 + 4 * lane;
+    load4_shared(pk, z);
+    if (ratio == 2) load4_shared(pk + 128, zy);
   }
   if (ratio == 2) {
 #pragma unroll
@@ -167,8 +206,27 @@ __device__ __forceinline__ void append_block(const Tin* __restrict__ lat, const 
                                              int32_t* __restrict__ len, int64_t cap, int n_new, int bx, int b,
                                              bool own_len) {
   const int lane = threadIdx.x & 31;
-  const int64_t base = len[b];  // in flight while the first entry is packed
+  const int64_t base = len[b];  // in flight while the tokens are copied
   __shared__ MergeWeights W;
+  __shared__ unsigned long long stage_bar;
+  __shared__ int stage_abort;
+  extern __shared__ __align__(16) unsigned char append_stage[];
+  Tin* st_lat = reinterpret_cast<Tin*>(append_stage);            // [ratio * kAppendBlockEntries][512]
+  Tin* st_key = st_lat + (size_t)ratio * kAppendBlockEntries * 512;  // [ratio * kAppendBlockEntries][128]
+  const int e_begin = bx * kAppendBlockEntries;
+  const int ntok = max(0, min(kAppendBlockEntries, n_new - e_begin)) * ratio;
+  const uint32_t sbar = smem_u32(&stage_bar);
+  if (threadIdx.x == 0 && ntok > 0) {
+    mbar_init(sbar, 1);
+    stage_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    const size_t tok0 = (size_t)b * T + (size_t)e_begin * ratio;
+    const uint32_t nlat = (uint32_t)ntok * 512u * (uint32_t)sizeof(Tin), nkey = (uint32_t)ntok * 128u * (uint32_t)sizeof(Tin);
+    const uint64_t pol = l2_evict_first_policy();
+    mbar_arrive_expect_tx(sbar, nlat + nkey);
+    bulk_load(smem_u32(st_lat), lat + tok0 * 512, nlat, sbar, pol);
+    bulk_load(smem_u32(st_key), ikey + tok0 * 128, nkey, sbar, pol);
+  }
   if (ratio == 2) {  // the block loads the weights once (16-byte vectors), transposing them
     for (int i = threadIdx.x; i < 2 * 512 / 4; i += blockDim.x) {
       const float4 v = __ldg(reinterpret_cast<const float4*>(i < 128 ? w0l : w1l) + (i & 127));
@@ -186,7 +244,11 @@ __device__ __forceinline__ void append_block(const Tin* __restrict__ lat, const 
 #pragma unroll
       for (int u = 0; u < 4; ++u) dst[((c0 + u) & 3) * 32 + ((c0 + u) >> 2)] = vv[u];
     }
-    __syncthreads();
+  }
+  __syncthreads();  // the weights and the barrier's initialisation
+  if (ntok > 0 && !mbar_wait_bounded(sbar, 0u, &stage_abort)) {
+    volatile int again = 0;  // a wait ran out (recorded): let the copy land before going on
+    mbar_wait_bounded(sbar, 0u, &again);
   }
   const bool refused = base < 0 || base + n_new > cap;  // the whole append of this sequence is refused
   if (refused && bx == 0 && threadIdx.x == 0) set_dev_error(CSA2_ERR_BOUNDS);
@@ -195,7 +257,7 @@ __device__ __forceinline__ void append_block(const Tin* __restrict__ lat, const 
   for (int j = 0; j < kAppendPerWarp; ++j) {
     const int e = e0 + j * kAppendWarps;
     if (e >= n_new) break;
-    const PackedLane P = quant_entry(lat, ikey, T, ratio, W, b, e, lane);
+    const PackedLane P = quant_entry(st_lat, st_key, (e - e_begin) * ratio, ratio, W, lane);
     if (!refused)
       store_entry(P, lat_codes, lat_scales, idx_codes, idx_scales, (int64_t)b * cap + base + e, lane);
   }
@@ -203,6 +265,12 @@ __device__ __forceinline__ void append_block(const Tin* __restrict__ lat, const 
     __syncthreads();
     if (threadIdx.x == 0 && !refused) len[b] = (int32_t)(base + n_new);
   }
+}
+
+// Dynamic shared memory of an append block: its source tokens (latent and key rows).
+template <typename Tin>
+constexpr size_t append_stage_bytes(int ratio) {
+  return (size_t)ratio * kAppendBlockEntries * (512 + 128) * sizeof(Tin);
 }
 
 template <typename Tin>
