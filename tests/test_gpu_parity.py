@@ -348,3 +348,23 @@ def test_topk_large_rows(n, k):
     for b in range(B):
         ref = O.topk_positions(s[b].numpy().astype(np.float64), k)
         assert np.array_equal(np_(out[b]), ref)
+
+
+@pytest.mark.parametrize("k,scale", [(512, 2.0 ** -12), (0, 2.0 ** -12), (512, 2.0 ** 12), (0, 2.0 ** 12)])
+def test_attention_window_magnitudes_within_2e3(k, scale):
+    """bf16 window rows far from unit scale but inside the fp16 range the window goes
+    through: 2^-12 N(0,1) (many values fp16 subnormals) and 2^12 N(0,1) (up to about
+    2e4), with and without selected entries."""
+    B, N, H, W = 2, 1200, 64, 128
+    cache, host = _small_cache(B, N, seed=6)
+    q, _, _ = WL.queries(6, "attn", B, H, dtype=torch.bfloat16, device="cuda")
+    rows = (WL.window(6, 0, B, W, device="cuda").float() * scale).to(torch.bfloat16)
+    rng = np.random.default_rng(k + 7)
+    idx = np.stack([np.sort(rng.choice(N, k, replace=False)) for _ in range(B)]).astype(np.int32) if k else None
+    out = K.sparse_latent_attn(q, cache, torch.from_numpy(idx).cuda() if k else None, swa=rows)
+    torch.cuda.synchronize()
+    assert K.sync_status() == 0
+    for b in range(B):
+        ref = O.attend(np_(q[b]).astype(np.float64), host.lat_codes[b], host.lat_scales[b],
+                       idx[b] if k else -np.ones(1, np.int64), np_(rows[b]).astype(np.float64))
+        assert Hh.attn_rel_err(np_(out[b]), ref) <= Hh.ATTN_TOL, b
