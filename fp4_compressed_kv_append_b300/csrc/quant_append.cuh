@@ -26,7 +26,7 @@
 namespace csa2 {
 
 constexpr int kAppendWarps = 8;
-constexpr int kAppendPerWarp = 4;
+constexpr int kAppendPerWarp = 2;  // 16 entries a block: a 40 KB stage (bf16, ratio 2), four blocks per SM
 constexpr int kAppendBlockEntries = kAppendWarps * kAppendPerWarp;
 
 // Lane l's share of one packed entry.
@@ -274,7 +274,7 @@ constexpr size_t append_stage_bytes(int ratio) {
 }
 
 template <typename Tin>
-__global__ void __launch_bounds__(kAppendWarps * 32, 3)
+__global__ void __launch_bounds__(kAppendWarps * 32, 4)
 k_quant_append(const Tin* __restrict__ lat, const Tin* __restrict__ ikey, int T, int ratio,
                const float* __restrict__ w0l, const float* __restrict__ w1l,
                const float* __restrict__ w0i, const float* __restrict__ w1i,
@@ -310,7 +310,7 @@ struct StoreArgs {
 };
 
 template <typename Tin>
-__global__ void __launch_bounds__(kAppendWarps * 32, 3) k_store_append(const __grid_constant__ StoreArgs a) {
+__global__ void __launch_bounds__(kAppendWarps * 32, 4) k_store_append(const __grid_constant__ StoreArgs a) {
   pdl_wait_and_release();
   int l = 0;
   for (int i = 1; i < a.n_layers; ++i)
