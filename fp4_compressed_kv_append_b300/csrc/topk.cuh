@@ -9,12 +9,15 @@
 // equal keys the lower slot wins. Slots past the row's length, and candidate
 // slots holding -1, are invalid and never selected.
 //
-// One cluster of kTopkCluster blocks per row; block r owns slice r of the row and
-// each of its threads a contiguous run of the slice. Radix select over the
+// One cluster of CLUSTER blocks of THREADS threads per row (the shape is a template
+// parameter; the launcher picks it by row length); block r owns slice r of the row
+// and each of its threads a contiguous run of the slice. Radix select over the
 // cluster:
 //  0. every block reads its slice once (kept as keys in shared memory when the
-//     slice has at most kRxSliceCap slots, else re-read from global memory by each
-//     pass) and publishes its valid count and key range to every block;
+//     slice has at most kRxSliceCap = 36 x THREADS slots, else re-read from global
+//     memory by each pass: coalesced 16-byte chunks for the passes whose order does
+//     not matter, rounds of four consecutive chunks a thread for the ordered ones)
+//     and publishes its valid count and key range to every block;
 //  1. if the row has at most k valid slots they are all selected. Otherwise:
 //  1a. a bound first: every thread also keeps the largest key it read, and block r
 //     finds lb_r, the lower edge of the bin (one fitted histogram level over its
@@ -92,7 +95,7 @@ struct alignas(16) TopkCtl {
 
 // Shared memory of a shape: the control block, the kept keys (kSliceCap), their
 // valid bits (one 64-bit word per thread) and block 0's gathered list (keys, slots):
-// 109 KB for 512 threads (two blocks per SM).
+// 109 KB for 512 threads (two blocks per SM), 186 KB for 1,024 (one).
 template <int THREADS, int CLUSTER>
 constexpr size_t topk_smem() {
   static_assert(sizeof(TopkCtl<THREADS, CLUSTER>) % 16 == 0,
