@@ -336,10 +336,16 @@ def test_topk_unrepresentative_sample_takes_the_exact_fallback(sampled_high):
         assert np.array_equal(np_(out[b]), ref)
 
 
-# rows around the longest one kept in shared memory (8 x 18,432 = 147,456 slots), one
-# that is just too long for some blocks, and one of the decode cache's appended lengths
+# rows at every cluster shape's limit and just past it (four 512-thread blocks up to
+# 73,728 slots, eight up to 147,456, sixteen 1,024-thread blocks up to 589,824, then
+# sixteen 512-thread blocks re-reading their slices: coalesced unordered passes,
+# ordered rounds for the list gather (k = 512) and the output (k = 16,384)), and one
+# of the decode cache's appended lengths; heavy ties send the bounded select to the
+# histogram levels
 @pytest.mark.parametrize("n,k", [(524288, 16384), (65536 + 77, 512), (20000, 1500), (147456, 512),
-                                 (147456 + 13, 512), (135200, 512), (300001, 2048)])
+                                 (147456 + 13, 512), (135200, 512), (300001, 2048), (73728, 512),
+                                 (73728 + 4, 512), (589824, 512), (589824 + 8, 2048), (600000, 512),
+                                 (600003, 16384)])
 def test_topk_large_rows(n, k):
     B = 2
     s = WL.scores(n + k, B, n, device="cpu", ties=100000)
