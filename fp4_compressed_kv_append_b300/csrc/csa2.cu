@@ -366,10 +366,19 @@ void launch_attn_cl(const AttnLayer* L, int nl, csa2_dtype dt, int H, float scal
     t.swa_scales[i] = L[i].win.scales;
     t.out[i] = L[i].out;
   }
-  const int C = (k + W + kAclKeys - 1) / kAclKeys;
+  // C blocks per (sequence, 64 heads, layer): one 128-key chunk each while the rows fill
+  // fewer than one block per SM, else fewer blocks with several chunks each (down to one
+  // block a row: no merge). fp32 queries keep one chunk per block.
+  const int c_full = (k + W + kAclKeys - 1) / kAclKeys;
+  int C = c_full;
+  if (NPART == 1) {
+    const int64_t rows = (int64_t)(H / kAclHeads) * c.batch * nl;
+    const int64_t per = (int64_t)sm_count() / (rows > 0 ? rows : 1);
+    C = (int)(per < 1 ? 1 : per < c_full ? per : c_full);
+  }
   launch_k(k_sparse_attn_cl<NPART>, dim3((unsigned)(C * (H / kAclHeads)), (unsigned)c.batch, (unsigned)nl),
-           dim3(kAclThreads), kAclSmem, s, (unsigned)C, t, (int)dt, scale, c.lat_codes, c.lat_scales, c.len, c.cap,
-           k, W, H, q_early);
+           dim3(kAclThreads), kAclSmem, s, C > 1 ? (unsigned)C : 0u, t, (int)dt, scale, c.lat_codes, c.lat_scales,
+           c.len, c.cap, k, W, H, q_early, C);
 }
 
 // The key-split form covers 64-head groups and up to 1,024 keys per row; the

@@ -374,3 +374,39 @@ def test_attention_window_magnitudes_within_2e3(k, scale):
         ref = O.attend(np_(q[b]).astype(np.float64), host.lat_codes[b], host.lat_scales[b],
                        idx[b] if k else -np.ones(1, np.int64), np_(rows[b]).astype(np.float64))
         assert Hh.attn_rel_err(np_(out[b]), ref) <= Hh.ATTN_TOL, b
+
+
+@pytest.mark.parametrize("per_row,W,qscale,win,dtype", [
+    (1, 128, 1.0, "bf16", torch.bfloat16), (1, 128, 64.0, "bf16", torch.bfloat16),
+    (1, 128, 64.0, "fp8", torch.bfloat16), (1, 0, 64.0, None, torch.bfloat16),
+    (2, 128, 64.0, "bf16", torch.bfloat16), (3, 0, 64.0, None, torch.bfloat16),
+    (1, 128, 64.0, "bf16", torch.float32)])
+def test_attention_rows_beyond_the_sms_within_2e3(per_row, W, qscale, win, dtype):
+    """More (sequence, 64-head) rows than SMs / per_row: the key-split form gives each
+    row per_row blocks that take several 128-key chunks each (one block a row, no
+    merge, at per_row = 1), with a running softmax per head. Queries scaled by 2^6
+    make the softmax peaked, so later chunks pass a head's reference by more than
+    2^8 and the accumulated O and sum are rescaled. fp32 queries keep one chunk per
+    block whatever the row count."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B = sms + 12 if per_row == 1 else sms // per_row
+    N, H, k, seed = 640, 64, 512, 8
+    cache = Hh.build_gpu_cache("lognormal", seed, B, N, 1, N)
+    q, _, _ = WL.queries(seed, "attn", B, H, dtype=dtype, device="cuda")
+    q = (q.float() * qscale).to(dtype)  # a power of two: exact in either type
+    rng = np.random.default_rng(per_row * 1000 + W + int(qscale))
+    idx = np.stack([np.sort(rng.choice(N, k, replace=False)) for _ in range(B)]).astype(np.int32)
+    rows = WL.window(seed, 0, B, W, device="cuda") if W else None
+    swa = rows if win == "bf16" else K.swa_quant(rows) if win == "fp8" else None
+    out = K.sparse_latent_attn(q, cache, torch.from_numpy(idx).cuda(), swa=swa)
+    torch.cuda.synchronize()
+    assert K.sync_status() == 0
+    for b in sorted({0, 1, B // 2, B - 2, B - 1} | set(rng.choice(B, 5, replace=False).tolist())):
+        host = Hh.host_cache_from_rows([Hh.oracle_cache_rows("lognormal", seed, b, N, 1)], N)
+        wref = None
+        if win == "bf16":
+            wref = np_(rows[b]).astype(np.float64)
+        elif win == "fp8":
+            wref = O.dequantize_swa(*O.quantize_swa(np_(rows[b])))
+        ref = O.attend(np_(q[b]).astype(np.float64), host.lat_codes[0], host.lat_scales[0], idx[b], wref)
+        assert Hh.attn_rel_err(np_(out[b]), ref) <= Hh.ATTN_TOL, b
