@@ -16,7 +16,7 @@
 //    hi + lo, the lo part kept in registers) are staged once in shared memory and
 //    serve every chunk;
 //  * per chunk: thread t holds a quarter of key t/4 (64 code bytes, 8 E4M3 bytes,
-//    loaded while the previous chunk was being computed) and dequantises it to fp16
+//    loaded while the previous chunk's S^T was on the tensor cores) and dequantises it to fp16
 //    (exact) into V; S^T = V Q^T on the 5th-generation tensor cores (one thread
 //    issues 32 tcgen05.mma, M = 128 keys, N = 64 heads, K = 16 each, into tensor
 //    memory; fp32 queries: a second pass with the fp16 remainder); the logits are
@@ -365,11 +365,6 @@ k_sparse_attn_cl(const __grid_constant__ AclLayers layers, int q_dtype, float sc
         *reinterpret_cast<uint4*>(vs + acl_vidx(kk, 2 * (4 * (i >> 1) + qq) + (i & 1))) = make_uint4(0, 0, 0, 0);
     }
     if (qq == 0) key_ok[kk] = kind != 0 ? 1 : 0;
-    if (t + 1 < nch) {  // the next chunk's codes and scales, and the selection after it
-      const int p = pos_next;
-      pos_next = read_sel(t + 2);
-      load_keys(t + 1, p);
-    }
 
     // ---- S^T = V Q^T on the tensor cores (tcgen05, M = 128 keys, N = 64 heads, K = 512
     // in 32 steps): one thread issues, the accumulator lives in tensor memory
@@ -405,6 +400,11 @@ k_sparse_attn_cl(const __grid_constant__ AclLayers layers, int q_dtype, float sc
         }
         tc_commit(bar);
         *n_commits = *n_commits + 1;
+      }
+      if (part == NPART - 1 && t + 1 < nch) {  // while the MMAs run: the next chunk's codes and
+        const int p = pos_next;                // scales, and the selection after it
+        pos_next = read_sel(t + 2);
+        load_keys(t + 1, p);
       }
       mbar_wait_bounded(bar, n_wait & 1u, abort);  // the MMAs are done reading Q and V (or abort is set)
       ++n_wait;
