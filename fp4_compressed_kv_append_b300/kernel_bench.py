@@ -5,11 +5,14 @@
 
 Kernels: scan (indexer_score over every entry), topk (topk_select, k = 512),
 attn (sparse_latent_attn over 512 selected entries), append (kv_quant_append of
-one token per sequence), step (one Full-layer csa2_decode_step). The launches are
+one token per sequence), write (kv_quant_append of 2 x --entries bf16 tokens of one
+sequence at ratio 2, the cache length reset before each launch), step (one
+Full-layer csa2_decode_step). The launches are
 captured in a CUDA graph, each between two CUDA events; with --flush a 256 MB
 buffer is written between launches so that L2 holds nothing of the inputs. Prints one JSON
 line per kernel: average microseconds per launch, algorithmic bytes per launch
-(68 per scanned entry, 288 per gathered entry, 4 per score read by Top-k) and
+(68 per scanned entry, 288 per gathered entry, 4 per score read by Top-k, 2,560
+in + 356 out per written entry) and
 the resulting GB/s.
 """
 from __future__ import annotations
@@ -64,7 +67,7 @@ def time_launches(fn, iters, warmup, flush):
 
 def main():
     p = argparse.ArgumentParser()
-    p.add_argument("--kernel", default="all", choices=["all", "scan", "topk", "attn", "append", "step"])
+    p.add_argument("--kernel", default="all", choices=["all", "scan", "topk", "attn", "append", "write", "step"])
     p.add_argument("--batch", type=int, default=32)
     p.add_argument("--entries", type=int, default=131072)
     p.add_argument("--heads", type=int, default=64)
@@ -92,6 +95,14 @@ def main():
         cache.len.fill_(N - 1)  # the appended token rewrites the last row each launch
         runs["append"] = (lambda: (cache.len.fill_(N - 1), kv_quant_append(tok[0], tok[1], 1, cache)),
                           (2048 + 512 + 356) * B)
+    if a.kernel == "write":  # one ratio-2 bulk append (bf16 sources with outlier channels)
+        lat, ikey = WL.outlier_tokens(0, 0, 2 * N, device="cuda")
+        wcache = Cache(1, (N + 127) // 128 * 128)
+        mw = WL.merge_weights(0, device="cuda")
+        zero = torch.zeros_like(wcache.len)
+        runs = {"write": (lambda: (wcache.len.copy_(zero),
+                                   kv_quant_append(lat[None], ikey[None], 2, wcache, *mw)),
+                          (2560 + 356) * N)}
     if a.kernel in ("step", "all"):
         step = DecodeStep([Layer(FULL, q, out, cache=cache, q_idx=q_idx, w_idx=w)], k)
         runs["step"] = (step, 68 * B * N + 288 * B * k)
